@@ -1,0 +1,417 @@
+"""Pins of the CPU oracle against things other than itself (CPU only).
+
+Each check below ties one oracle function to what the pages or mathematics fix: the worked example
+printed on the Expert-Parallelism lesson page, brute force on tiny inputs, closed forms, and
+special cases that reduce to a library routine. The mutation tests at the end plant a plausible
+mistake in the oracle (on the CPU) and show that a pin fails on it.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle.moe_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------- worked example
+def check_worked_example(mod):
+    with open(os.path.join(GOLDEN, "worked_example.json")) as f:
+        g = json.load(f)
+    epr = g["experts_per_rank"]
+    for case in g["cases"]:
+        loads = mod.load_per_rank(case["tokens_per_expert"], epr)
+        assert loads == case["rank_loads"]
+        assert round(mod.imbalance(loads), 2) == pytest.approx(case["imbalance"])
+        if "routing_volume_tokens" in case:
+            assert mod.routing_volume(case["tokens_per_expert"]) == case["routing_volume_tokens"]
+            assert mod.utilisation(loads) == pytest.approx(case["utilisation_num"] / case["utilisation_den"])
+    m = mod.expert_to_rank(g["expert_to_rank"]["num_experts"], g["expert_to_rank"]["experts_per_rank"])
+    assert all(m[e] == e // 32 for e in range(256))
+    assert m[31] == 0 and m[32] == 1 and m[255] == 7
+
+
+def test_worked_example():
+    check_worked_example(O)
+
+
+def test_imbalance_rejects_empty():
+    with pytest.raises(ValueError):
+        O.imbalance([0, 0])
+
+
+# ----------------------------------------------------------------------------- Top-K brute force
+def brute_topk(keys_row, K, eligible_row):
+    """The unique K-subset S with: for all i in S, eligible j not in S, key_i > key_j or
+    (key_i == key_j and i < j); listed by (key desc, index asc)."""
+    E = len(keys_row)
+    elig = [e for e in range(E) if eligible_row[e]]
+    winners = []
+    for S in itertools.combinations(elig, K):
+        rest = [j for j in elig if j not in S]
+        if all(keys_row[i] > keys_row[j] or (keys_row[i] == keys_row[j] and i < j) for i in S for j in rest):
+            winners.append(S)
+    assert len(winners) == 1, winners
+    return sorted(winners[0], key=lambda e: (-keys_row[e], e))
+
+
+def check_topk_bruteforce(mod):
+    rng = np.random.default_rng(1)
+    for trial in range(300):
+        E = int(rng.integers(2, 9))
+        K = int(rng.integers(1, min(3, E) + 1))
+        T = 4
+        keys = rng.integers(-2, 3, size=(T, E)).astype(np.float64)  # many ties
+        if trial % 3 == 0:
+            keys = rng.standard_normal((T, E))
+        got = mod.topk(keys, K)
+        for t in range(T):
+            assert list(got[t]) == brute_topk(list(keys[t]), K, [True] * E)
+
+
+def test_topk_bruteforce():
+    check_topk_bruteforce(O)
+
+
+def test_topk_all_equal_and_infinities():
+    keys = np.zeros((2, 6))
+    assert O.topk(keys, 3).tolist() == [[0, 1, 2], [0, 1, 2]]
+    keys = np.array([[-np.inf, 1.0, -np.inf, 1.0]])
+    assert O.topk(keys, 3).tolist() == [[1, 3, 0]]
+    with pytest.raises(ValueError):
+        O.topk(np.array([[np.nan, 0.0]]), 1)
+
+
+# ----------------------------------------------------------------------------- group limit brute force
+def brute_group(keys_row, n_groups, topk_groups, K):
+    E = len(keys_row)
+    gs = E // n_groups
+    score = []
+    for g in range(n_groups):
+        ks = keys_row[g * gs:(g + 1) * gs]
+        if gs == 1:
+            score.append(ks[0])
+        else:
+            score.append(max(ks[i] + ks[j] for i in range(gs) for j in range(gs) if i < j))
+    winners = []
+    for G in itertools.combinations(range(n_groups), topk_groups):
+        rest = [h for h in range(n_groups) if h not in G]
+        if all(score[a] > score[b] or (score[a] == score[b] and a < b) for a in G for b in rest):
+            winners.append(G)
+    assert len(winners) == 1
+    elig = [(e // gs) in winners[0] for e in range(E)]
+    return brute_topk(list(keys_row), K, elig)
+
+
+def check_group_bruteforce(mod):
+    rng = np.random.default_rng(2)
+    for trial in range(200):
+        n_groups = int(rng.choice([2, 4]))
+        gs = int(rng.choice([1, 2, 3]))
+        E = n_groups * gs
+        topk_groups = int(rng.integers(1, n_groups + 1))
+        K = int(rng.integers(1, topk_groups * gs + 1))
+        keys = rng.integers(-2, 3, size=(3, E)).astype(np.float64)
+        if trial % 2:
+            keys = rng.standard_normal((3, E))
+        elig = mod.group_limit(keys, n_groups, topk_groups)
+        got = mod.topk(keys, K, elig)
+        for t in range(3):
+            assert list(got[t]) == brute_group(list(keys[t]), n_groups, topk_groups, K)
+
+
+def test_group_limit_bruteforce():
+    check_group_bruteforce(O)
+
+
+def test_group_limit_binds():
+    # Group 0 holds the single best expert but group 1 has the better top-2 sum.
+    keys = np.array([[5.0, -9.0, 3.0, 3.0]])
+    elig = O.group_limit(keys, 2, 1)
+    assert elig.tolist() == [[False, False, True, True]]
+    assert O.topk(keys, 2, elig).tolist() == [[2, 3]]
+
+
+# ----------------------------------------------------------------------------- capacity brute force
+def check_dispatch_bruteforce(mod):
+    rng = np.random.default_rng(3)
+    for trial in range(60):
+        E = int(rng.integers(1, 7))
+        K = int(rng.integers(1, E + 1))
+        T = int(rng.integers(0, 13))
+        idx = np.array([rng.permutation(E)[:K] for _ in range(T)], dtype=np.int32).reshape(T, K)
+        C = None if trial % 4 == 0 else int(rng.integers(1, 5))
+        d = mod.dispatch(idx, E, C)
+        # brute force: rank(t,k) = number of earlier units that picked the same expert
+        rank = np.zeros((T, K), dtype=int)
+        for t in range(T):
+            for k in range(K):
+                rank[t, k] = sum(1 for t2 in range(t) for k2 in range(K) if idx[t2, k2] == idx[t, k])
+        cnt = [int((idx == e).sum()) for e in range(E)]
+        kept = [c if C is None else min(c, C) for c in cnt]
+        off = [sum(kept[:e]) for e in range(E + 1)]
+        assert d.counts.tolist() == cnt
+        assert d.kept.tolist() == kept
+        assert d.offsets.tolist() == off
+        for t in range(T):
+            for k in range(K):
+                e = idx[t, k]
+                if C is None or rank[t, k] < C:
+                    assert d.slot_of[t, k] == off[e] + rank[t, k]
+                    assert d.row_token[d.slot_of[t, k]] == t
+                else:
+                    assert d.slot_of[t, k] == -1
+        # invariants: every kept pick appears once; rows past kept are -1
+        s = d.slot_of[d.slot_of >= 0]
+        assert len(np.unique(s)) == len(s) == off[E]
+        assert (d.row_token[off[E]:] == -1).all()
+        assert sum(cnt) == T * K
+
+
+def test_dispatch_bruteforce():
+    check_dispatch_bruteforce(O)
+
+
+def test_capacity_values():
+    # C = CF·K·T/E from the capacity passage; the two dropping workloads give integers.
+    assert O.capacity(1.25, 2, 256, 8) == 80
+    assert O.capacity(1.25, 2, 16384, 64) == 640
+    assert O.capacity(None, 2, 256, 8) is None
+    assert O.capacity(0.0, 2, 256, 8) is None
+    assert O.capacity(float("inf"), 2, 256, 8) is None
+    assert O.capacity(1.2, 2, 256, 8) == 77  # 76.8 rounds up
+
+
+def test_capacity_one_keeps_first_unit():
+    idx = np.array([[0, 1], [1, 2], [0, 2], [2, 0]], dtype=np.int32)
+    d = O.dispatch(idx, 3, 1)
+    assert d.slot_of.tolist() == [[0, 1], [-1, 2], [-1, -1], [-1, -1]]
+    assert d.row_token.tolist()[:3] == [0, 0, 1]
+
+
+# ----------------------------------------------------------------------------- gates, aux
+def check_gates(mod):
+    rng = np.random.default_rng(4)
+    l = rng.standard_normal((50, 8)) * 3
+    idx, g, _ = mod.route(l, "softmax", 3)
+    p = scipy.special.softmax(l, axis=1)
+    pk = np.take_along_axis(p, idx.astype(int), axis=1)
+    np.testing.assert_allclose(g, pk / pk.sum(axis=1, keepdims=True), rtol=1e-13)
+    np.testing.assert_allclose(g.sum(axis=1), 1.0, rtol=1e-14)
+    assert (np.diff(g, axis=1) <= 0).all()  # descending key order = descending gate for softmax
+    idx, g, _ = mod.route(l, "sigmoid", 3)
+    s = scipy.special.expit(l)
+    sk = np.take_along_axis(s, idx.astype(int), axis=1)
+    np.testing.assert_allclose(g, sk / sk.sum(axis=1, keepdims=True), rtol=1e-13)
+
+
+def test_gates():
+    check_gates(O)
+
+
+def test_sigmoid_bias_selects_but_does_not_weight():
+    l = np.array([[2.0, 1.0, 0.0]])
+    b = np.array([0.0, 0.0, 0.9])
+    idx, g, keys = O.route(l, "sigmoid", 2, select_bias=b)
+    assert idx.tolist() == [[2, 0]]  # σ(0)+0.9 = 1.4 > σ(2) = 0.88 > σ(1) = 0.73
+    s = scipy.special.expit(np.array([0.0, 2.0]))
+    np.testing.assert_allclose(g[0], s / s.sum(), rtol=1e-14)
+
+
+def check_aux_uniform(mod):
+    # Circulant logits: unit t has l[t,e] = v[(e - t) mod E] → every expert is picked T'K/E times
+    # and P_i = 1/E by symmetry, so L_aux = α·E·Σ (1/E)(1/E) = α.
+    E, K, alpha = 8, 2, 0.01
+    v = np.array([3.0, 1.5, 0.2, -0.4, 0.9, -2.0, 0.0, 0.7])
+    T = 5 * E
+    l = np.array([[v[(e - t) % E] for e in range(E)] for t in range(T)])
+    for score in ("softmax", "sigmoid"):
+        idx, _, _ = mod.route(l, score, K)
+        assert mod.aux_loss(l, idx, E, K, alpha, score) == pytest.approx(alpha, rel=1e-12)
+
+
+def test_aux_uniform_equals_alpha():
+    check_aux_uniform(O)
+
+
+def check_aux_hand(mod):
+    # Two units, both picking expert 1 of 2: f = [0, 1]; P = softmax([0, ln 3]) = [1/4, 3/4].
+    # L_aux = α·2·(0·1/4 + 1·3/4) = 1.5α.
+    l = np.array([[0.0, math.log(3.0)], [0.0, math.log(3.0)]])
+    idx, _, _ = mod.route(l, "softmax", 1)
+    assert idx.tolist() == [[1], [1]]
+    assert mod.aux_loss(l, idx, 2, 1, 0.01, "softmax") == pytest.approx(0.015, rel=1e-12)
+
+
+def test_aux_hand_value():
+    check_aux_hand(O)
+
+
+# ----------------------------------------------------------------------------- expert FFN and the layer
+def _rand_layer(rng, T, h, E, d_ff):
+    x = rng.standard_normal((T, h))
+    wg = rng.standard_normal((h, E)) / math.sqrt(h)
+    W1 = rng.standard_normal((E, d_ff, h)) / math.sqrt(h)
+    W3 = rng.standard_normal((E, d_ff, h)) / math.sqrt(h)
+    W2 = rng.standard_normal((E, h, d_ff)) / math.sqrt(d_ff)
+    return x, wg, W1, W3, W2
+
+
+def check_dense_single_expert(mod):
+    # E = 1, K = 1: the layer is one dense SwiGLU FFN; compare with torch's silu and matmul.
+    rng = np.random.default_rng(5)
+    x, wg, W1, W3, W2 = _rand_layer(rng, 7, 12, 1, 20)
+    r = mod.forward(x, wg, lambda e: (W1[e], W3[e], W2[e]), E=1, K=1)
+    tx = torch.from_numpy(x)
+    ref = (torch.nn.functional.silu(tx @ torch.from_numpy(W1[0]).T) * (tx @ torch.from_numpy(W3[0]).T)) \
+        @ torch.from_numpy(W2[0]).T
+    np.testing.assert_allclose(r.y, ref.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_dense_single_expert_is_swiglu():
+    check_dense_single_expert(O)
+
+
+def check_dense_mixture(mod):
+    # K = E, no drop: y = Σ_e softmax(l)_e · FFN_e(x) (softmax over all E = over the picks).
+    rng = np.random.default_rng(6)
+    x, wg, W1, W3, W2 = _rand_layer(rng, 9, 10, 4, 6)
+    r = mod.forward(x, wg, lambda e: (W1[e], W3[e], W2[e]), E=4, K=4)
+    p = scipy.special.softmax(x @ wg, axis=1)
+    ref = np.zeros_like(x)
+    for t in range(9):
+        for e in range(4):
+            hdn = scipy.special.expit(W1[e] @ x[t]) * (W1[e] @ x[t]) * (W3[e] @ x[t])
+            ref[t] += p[t, e] * (W2[e] @ hdn)
+    np.testing.assert_allclose(r.y, ref, rtol=1e-11, atol=1e-13)
+
+
+def test_dense_mixture():
+    check_dense_mixture(O)
+
+
+def test_router_logits_loop():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((3, 5))
+    wg = rng.standard_normal((5, 4))
+    b = rng.standard_normal(4)
+    l = O.router_logits(x, wg, b)
+    for t in range(3):
+        for e in range(4):
+            assert l[t, e] == pytest.approx(sum(x[t, i] * wg[i, e] for i in range(5)) + b[e], rel=1e-13)
+
+
+def test_silu_closed_form():
+    z = np.linspace(-30, 30, 121)
+    np.testing.assert_allclose(O.silu(z), torch.nn.functional.silu(torch.from_numpy(z)).numpy(), rtol=1e-14, atol=1e-300)
+    assert O.silu(np.array([0.0]))[0] == 0.0
+
+
+def test_head_split_equals_per_head_layers():
+    # H = 2 with no drop: each head slice is an independent layer on [T][h'].
+    rng = np.random.default_rng(8)
+    T, hu, E, K, H = 6, 4, 4, 2, 2
+    x = rng.standard_normal((T, H * hu))
+    wg = rng.standard_normal((hu, E)) / 2
+    W1 = rng.standard_normal((E, 8, hu)); W3 = rng.standard_normal((E, 8, hu)); W2 = rng.standard_normal((E, hu, 8))
+    ex = lambda e: (W1[e], W3[e], W2[e])
+    r = O.forward(x, wg, ex, E=E, K=K, n_heads=H)
+    for j in range(H):
+        rj = O.forward(x[:, j * hu:(j + 1) * hu], wg, ex, E=E, K=K)
+        np.testing.assert_allclose(r.y[:, j * hu:(j + 1) * hu], rj.y, rtol=1e-13)
+    # sub-token order is t·H + j
+    np.testing.assert_allclose(r.logits[1], x[0, hu:] @ wg, rtol=1e-13)
+
+
+def test_permutation_equivariance():
+    rng = np.random.default_rng(9)
+    x, wg, W1, W3, W2 = _rand_layer(rng, 11, 8, 4, 6)
+    ex = lambda e: (W1[e], W3[e], W2[e])
+    perm = rng.permutation(11)
+    a = O.forward(x, wg, ex, E=4, K=2).y
+    b = O.forward(x[perm], wg, ex, E=4, K=2).y
+    np.testing.assert_allclose(a[perm], b, rtol=1e-13)
+
+
+def test_sampled_forward_matches_full():
+    rng = np.random.default_rng(10)
+    x, wg, W1, W3, W2 = _rand_layer(rng, 20, 8, 4, 6)
+    ex = lambda e: (W1[e], W3[e], W2[e])
+    full = O.forward(x, wg, ex, E=4, K=2, capacity_factor=1.0)
+    samp = O.forward(x, wg, ex, E=4, K=2, capacity_factor=1.0, sample_units=np.array([0, 5, 19]))
+    for u in (0, 5, 19):
+        np.testing.assert_allclose(samp.y_units[u], full.y[u], rtol=1e-13, atol=1e-15)
+
+
+def test_full_drop_gives_zero():
+    # capacity 1 with all units on one expert: only unit 0 keeps its pick.
+    x = np.ones((4, 3))
+    wg = np.zeros((3, 2)); wg[:, 0] = 1.0
+    W = np.ones((2, 5, 3)); W2 = np.ones((2, 3, 5))
+    r = O.forward(x, wg, lambda e: (W[e], W[e], W2[e]), E=2, K=1, capacity_factor=0.5)
+    assert r.C == 1
+    assert (r.y[1:] == 0).all() and (r.y[0] != 0).all()
+
+
+def test_comm_volume():
+    # 2·Tokens·K·h·sizeof: the Mixtral-shaped workload moves 128 MiB through dispatch + combine.
+    assert O.comm_volume_bytes(4096, 2, 4096, 2) == 134217728
+
+
+# ----------------------------------------------------------------------------- planted mistakes
+def _topk_ties_high(keys, K, eligible=None):
+    E = keys.shape[1]
+    if eligible is None:
+        eligible = np.ones(keys.shape, bool)
+    neg_idx = np.broadcast_to(-np.arange(E), keys.shape)
+    return np.lexsort((neg_idx, -keys, ~eligible), axis=1)[:, :K].astype(np.int32)
+
+
+def _group_limit_max_only(keys, n_groups, topk_groups):
+    T, E = keys.shape
+    if n_groups <= 1:
+        return np.ones((T, E), bool)
+    score = keys.reshape(T, n_groups, -1).max(axis=2)
+    order = np.argsort(-score, axis=1, kind="stable")
+    chosen = np.zeros((T, n_groups), bool)
+    np.put_along_axis(chosen, order[:, :topk_groups], True, axis=1)
+    return np.repeat(chosen, E // n_groups, axis=1)
+
+
+MUTANTS = [
+    ("silu sign", "silu", lambda z: np.asarray(z, np.float64) / (1.0 + np.exp(np.asarray(z, np.float64))),
+     check_dense_single_expert),
+    ("up uses W1", "expert_ffn", lambda xe, w1, w3, w2: (O.silu(xe @ w1.T) * (xe @ w1.T)) @ w2.T,
+     check_dense_single_expert),
+    ("aux without E", "aux_loss",
+     lambda l, idx, E, K, a, s: float(a * np.sum(O.expert_counts(idx, E) / (l.shape[0] * K) * O.routing_probs(l, s).mean(0))),
+     check_aux_uniform),
+    ("aux post-softmax of picks", "routing_probs", lambda l, s: np.full(l.shape, 1.0 / l.shape[1]), check_aux_hand),
+    ("topk ties to higher index", "topk", _topk_ties_high, check_topk_bruteforce),
+    ("group score = max only", "group_limit", _group_limit_max_only, check_group_bruteforce),
+    ("gates not renormalised", "gates",
+     lambda l, idx, s: np.take_along_axis(scipy.special.softmax(l, axis=1), idx.astype(int), axis=1), check_gates),
+]
+
+
+@pytest.mark.parametrize("name,attr,fn,check", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(monkeypatch, name, attr, fn, check):
+    monkeypatch.setattr(O, attr, fn)
+    with pytest.raises(AssertionError):
+        check(O)
+
+
+def test_dispatch_pin_catches_le_capacity(monkeypatch):
+    real = O.dispatch
+
+    def wrong(idx, E, C):
+        return real(idx, E, None if C is None else C + 1)  # keeps rank == C (off by one)
+    monkeypatch.setattr(O, "dispatch", wrong)
+    with pytest.raises(AssertionError):
+        check_dispatch_bruteforce(O)
