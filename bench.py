@@ -1,0 +1,404 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE FFN layer forward (one JSON line on stdout, rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one forward of the whole layer (router → Top-K → capacity/dispatch → expert SwiGLU
+grouped GEMMs → combine, plus the aux loss) over one batch of the workload, inputs resident in
+HBM. Default workload: the Mixtral-shaped layer (T=4096, h=4096, E=8, K=2, d_ff=14336, bf16,
+softmax Top-2, no drop). `value` is tokens/s of the whole job (N replicas, one per GPU, each with
+its own batch: weak scaling). L2 is flushed (a 512 MiB write) between timed steps, outside the
+timed events.
+
+--impl reference times the CPU oracle (float64 numpy) on the host cores on a bounded sample of
+the same workload, scaled to tokens/s.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, Generator, bf16_bits_to_f32  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------ inputs
+def device_inputs(shape, device):
+    from mixture_experts_layer_96_b300 import LayerWeights
+    g = Generator(shape, seed=0)
+    bf = shape.dtype == "bf16"
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if bf else torch.from_numpy(a)
+        return t.to(device)
+
+    x_host = g.x()
+    w1, w3, w2 = g.experts()
+    lb, sb = g.logit_bias(), g.select_bias()
+    lw = LayerWeights(dev(g.w_router()), dev(w1), dev(w3), dev(w2),
+                      None if lb is None else torch.from_numpy(lb).to(device),
+                      None if sb is None else torch.from_numpy(sb).to(device))
+    del w1, w3, w2
+    return dev(x_host), lw
+
+
+def kept_rows(shape):
+    if shape.capacity_factor is None:
+        return shape.T_units * shape.K
+    return None  # data-dependent; read back after a run
+
+
+# ------------------------------------------------------------------------------------ CPU oracle
+class OracleRun:
+    """The oracle on a bounded sample: it routes all units (capacity is global), then computes the
+    experts and the combine for `n_sample` units. Inputs (and the float64 widening of the expert
+    weights the sample needs) are prepared once, untimed, like resident inputs on the GPU."""
+
+    def __init__(self, shape, n_sample: int, seed: int = 0):
+        import oracle.moe_oracle as O
+        self.O = O
+        self.shape = shape
+        g = Generator(shape, seed)
+        bf = shape.dtype == "bf16"
+        f64 = (lambda a: bf16_bits_to_f32(a).astype(np.float64)) if bf else (lambda a: np.asarray(a, np.float64))
+        self.x = f64(g.x())
+        self.wg = f64(g.w_router())
+        self.kw = dict(E=shape.E, K=shape.K, score=shape.score, n_heads=shape.n_heads, n_groups=shape.n_groups,
+                       topk_groups=shape.topk_groups, capacity_factor=shape.capacity_factor,
+                       aux_alpha=shape.aux_alpha, logit_bias=g.logit_bias(), select_bias=g.select_bias())
+        rng = np.random.default_rng(1)
+        self.n = n_sample
+        self.sample = np.sort(rng.choice(shape.T_units, size=n_sample, replace=False))
+        r = O.forward(self.x, self.wg, lambda e: None, sample_units=self.sample[:0], **self.kw)
+        need = sorted({int(e) for u in self.sample for e in r.idx[u]})
+        self.cache = {}
+        for e in need:
+            w1, w3, w2 = g.expert(e)
+            self.cache[e] = (f64(w1), f64(w3), f64(w2))
+
+    def step(self):
+        """(seconds of the routing pass, seconds per sampled unit of experts + combine)."""
+        O = self.O
+        t0 = time.perf_counter()
+        O.forward(self.x, self.wg, lambda e: self.cache[e], sample_units=self.sample[:0], **self.kw)
+        t_route = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        O.forward(self.x, self.wg, lambda e: self.cache[e], sample_units=self.sample, **self.kw)
+        t_all = time.perf_counter() - t0
+        return t_route, max(t_all - t_route, 1e-9) / self.n
+
+    def full_batch_seconds(self, t_route, per_unit):
+        return t_route + per_unit * self.shape.T_units
+
+    def describe(self, t_route, per_unit):
+        s = self.shape
+        return (f"float64 numpy oracle: routing of all {s.T_units} units ({t_route:.3f} s) plus expert SwiGLU + "
+                f"combine for {self.n} sampled units ({per_unit:.3f} s/unit), scaled to the {s.T}-token batch; "
+                f"expert weights widened to float64 before timing")
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return int(max(n)) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline_leg(shape, n_sample):
+    run = OracleRun(shape, n_sample)
+    t_route, per_unit = run.step()
+    v = shape.T / run.full_batch_seconds(t_route, per_unit)
+    return {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": run.describe(t_route, per_unit)}
+
+
+# ------------------------------------------------------------------------------------ reference arm
+def run_reference(args, shape):
+    _, rank, _ = dist_env()
+    if rank != 0:
+        return
+    run = OracleRun(shape, args.ref_sample)
+    times, last = [], None
+    for i in range(args.warmup + args.steps):
+        t_route, per_unit = run.step()
+        if i >= args.warmup:
+            times.append(run.full_batch_seconds(t_route, per_unit))
+            last = (t_route, per_unit)
+    ms = 1000.0 * statistics.mean(times)
+    v = shape.T / (ms / 1000.0)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generator, the workload's recipe)",
+            "config": {"workload": shape.describe(), "global_batch": shape.T, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                             "sample": run.describe(*last)},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------ our arm
+def run_ours(args, shape):
+    from mixture_experts_layer_96_b300 import (ForwardOutputs, Workspace, launch_count, moe_combine,
+                                               moe_dispatch, moe_expert_ffn, moe_forward, moe_route)
+    from mixture_experts_layer_96_b300.moe import make_config
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    cfg = make_config(shape.T, shape.h, shape.E, shape.K, shape.d_ff, n_heads=shape.n_heads,
+                      n_groups=shape.n_groups, topk_groups=shape.topk_groups,
+                      capacity_factor=shape.capacity_factor, aux_alpha=shape.aux_alpha,
+                      score=shape.score, dtype=shape.dtype)
+    x, lw = device_inputs(shape, device)
+    ws = Workspace(cfg, device=device)
+    outs = ForwardOutputs(aux=torch.empty(1, dtype=torch.float32, device=device),
+                          counts=torch.empty(shape.E, dtype=torch.int32, device=device),
+                          offsets=torch.empty(shape.E + 1, dtype=torch.int32, device=device))
+    y = torch.empty_like(x)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        torch.cuda.synchronize(device)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    for _ in range(max(3, args.warmup)):
+        moe_forward(cfg, x, lw, ws=ws, y=y, outputs=outs)
+    ws.check()
+    kept = int(outs.offsets[-1].item())
+    aux = float(outs.aux.item())
+    counts = outs.counts.cpu().tolist()
+
+    # ---- timed: whole forward, one event pair per step, L2 flushed between steps (untimed)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    n0 = launch_count()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            moe_forward(cfg, x, lw, ws=ws, y=y, outputs=outs)
+            ev[i][1].record(stream)
+        barrier()
+    n_launch = launch_count() - n0
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ws.check()
+
+    # ---- per-stage events (same kernels through the stage entry points)
+    st = {k: [] for k in ("route", "dispatch", "expert_ffn", "combine")}
+    idx = torch.empty((shape.T_units, shape.K), dtype=torch.int32, device=device)
+    gate = torch.empty((shape.T_units, shape.K), dtype=torch.float32, device=device)
+    counts_t = torch.empty(shape.E, dtype=torch.int32, device=device)
+    offsets_t = torch.empty(shape.E + 1, dtype=torch.int32, device=device)
+    slot_of = torch.empty((shape.T_units, shape.K), dtype=torch.int32, device=device)
+    row_token = torch.empty(shape.T_units * shape.K, dtype=torch.int32, device=device)
+    xp = torch.empty((shape.T_units * shape.K, shape.h_unit), dtype=x.dtype, device=device)
+    yp = torch.empty_like(xp)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        e[0].record(stream)
+        moe_route(cfg, x, lw.w_router, lw.logit_bias, lw.select_bias, ws=ws, topk_idx=idx, topk_gate=gate,
+                  aux_out=outs.aux)
+        e[1].record(stream)
+        moe_dispatch(cfg, x, idx, ws=ws, counts=counts_t, offsets=offsets_t, slot_of=slot_of,
+                     row_token=row_token, x_packed=xp)
+        e[2].record(stream)
+        moe_expert_ffn(cfg, xp, offsets_t, lw.w_gate, lw.w_up, lw.w_down, ws=ws, y_packed=yp)
+        e[3].record(stream)
+        moe_combine(cfg, yp, slot_of, gate, ws=ws, y=y)
+        e[4].record(stream)
+        torch.cuda.synchronize(device)
+        for j, k in enumerate(st):
+            st[k].append(e[j].elapsed_time(e[j + 1]))
+    ws.check()
+    stage_ms = {k: statistics.mean(v) for k, v in st.items()}
+
+    # ---- e2e: pinned host x → device, forward, y → pinned host, every step
+    x_host = x.cpu().pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    aux_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        xd = x_host.to(device, non_blocking=True)
+        moe_forward(cfg, xd, lw, ws=ws, y=y, outputs=outs)
+        y_host.copy_(y, non_blocking=True)
+        aux_host.copy_(outs.aux, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = x_host.numel() * x_host.element_size()
+    d2h = y_host.numel() * y_host.element_size() + 4
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    # ---- roofline of the dominant kernel group (the expert grouped GEMMs)
+    pk = peaks()
+    flops = 6.0 * shape.h_unit * shape.d_ff * kept
+    achieved_tf = flops / (stage_ms["expert_ffn"] * 1e-3) / 1e12
+    peak_tf = float(pk["bf16_tflops"])
+    elt = 2 if shape.dtype == "bf16" else 4
+    d_bytes = shape.T_units * shape.h_unit * elt + kept * shape.h_unit * elt + kept * 4 * 2
+    c_bytes = kept * shape.h_unit * elt + shape.T_units * shape.h_unit * elt + shape.T_units * shape.K * 8
+    hbm = float(pk["hbm_gbs"])
+    stages = {
+        "route_ms": stage_ms["route"], "dispatch_ms": stage_ms["dispatch"],
+        "expert_ffn_ms": stage_ms["expert_ffn"], "combine_ms": stage_ms["combine"],
+        "expert_ffn_tflops": achieved_tf,
+        "dispatch_gbs": d_bytes / (stage_ms["dispatch"] * 1e-3) / 1e9,
+        "combine_gbs": c_bytes / (stage_ms["combine"] * 1e-3) / 1e9,
+    }
+    stages["dispatch_frac_hbm"] = stages["dispatch_gbs"] / hbm
+    stages["combine_frac_hbm"] = stages["combine_gbs"] / hbm
+    value = world * shape.T / (ms * 1e-3)
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if shape.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded generator; x~N(0,1), W~N(0,1/fan_in), bf16)",
+        "config": {"workload": shape.describe(), "global_batch": shape.T * world, "units_per_gpu": shape.T_units,
+                   "parallelism": f"replicas x{world} (data parallel, no collective on the data path)",
+                   "l2": "flushed between timed steps (512 MiB write, outside the events)",
+                   "kept_rows": kept, "aux_loss": aux, "max_over_mean_load": max(counts) / (sum(counts) / len(counts))},
+        "roofline": {"bound": "tensor", "kernel": "expert grouped GEMMs (gate/up+SwiGLU and down, 2 launches)",
+                     "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved_tf / peak_tf,
+                     "peak_kind": f"bf16 burst, {pk['source']}",
+                     "frac_of_sustained": achieved_tf / float(pk.get("bf16_tflops_sustained", peak_tf)),
+                     "traffic": None},
+        "stages": stages,
+        "clocks": clocks,
+        "e2e": {"value": shape.T * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": n_launch,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_leg(shape, args.cpu_sample)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixtral_bf16", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-sample", type=int, default=16, help="units the CPU-baseline oracle computes")
+    ap.add_argument("--ref-sample", type=int, default=2, help="units per reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    shape = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, shape)
+    else:
+        run_ours(args, shape)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * moe.h — C ABI of the single-GPU MoE FFN layer forward (B300, sm_103a).
+ *
+ * The layer, as the pages define it:
+ *   router logits  l = x·W_g                       [Lesson 10 "专家并行 EP", §1]
+ *   scores         Softmax(TopK(l, K)), or sigmoid  [Lesson 10 §1]
+ *                  (optionally a selection-only per-expert bias  [Chương 10 "Song song MoE", §4],
+ *                   and a group limit: a unit's K experts lie in at most M groups  [Lesson 10 §5])
+ *   capacity       C = CF·K·T/E, picks past C are dropped            [Lesson 10 §4]
+ *   dispatch       pack the units per expert                          [Lesson 10 §3, step 1]
+ *   expert FFN     per-expert grouped GEMM                            [Lesson 10 §3, step 2]
+ *   combine        y = Σ_{i∈TopK} s_i(x)·FFN_i(x), back in token order [Lesson 10 §1, §3 steps 3-4]
+ *   aux loss       L_aux = α·E·Σ_i f_i·P_i                             [Lesson 10 §4]
+ *   heads          x split into H heads, each routed independently     ["Multi-Head LatentMoE 与
+ *                                                                       Head 并行", 摘要 and 评论 §1]
+ * The expert is a SwiGLU FFN without biases: FFN_e(x) = W2_e·(silu(W1_e·x) ⊙ W3_e·x).
+ *
+ * Conventions shared by every call
+ *  - Ownership: the caller owns every buffer. All data pointers are DEVICE pointers (cudaMalloc'd
+ *    or torch tensors) unless a comment says otherwise. The library allocates no device memory
+ *    and frees none; scratch lives in the caller's workspace `ws` (size from
+ *    moe_workspace_size, 256-byte aligned, zeroed once by moe_workspace_init).
+ *  - Asynchrony: every compute call only enqueues kernels on `stream` and returns; it never
+ *    synchronises. moe_get_status is the one call that waits for the stream.
+ *  - Errors: invalid arguments are reported synchronously (MOE_ERR_INVALID_ARG /
+ *    MOE_ERR_UNSUPPORTED) and then nothing is enqueued. Faults the kernels detect in the data
+ *    (an expert index out of range, inconsistent offsets, a wait that timed out) set bits in a
+ *    status word inside `ws`; moe_get_status reports them. A kernel launch failure returns
+ *    MOE_ERR_CUDA.
+ *  - Layouts are row-major. A "unit" is a token (n_heads == 1) or a head sub-token: with H heads,
+ *    x[T][h] is read as T' = T·H units of width h' = h/H, unit t·H+j = x[t][j·h' .. (j+1)·h').
+ *    GEMM operands are K-major: W_gate/W_up [E][d_ff][h'], W_down [E][h'][d_ff]. The router weight
+ *    keeps the pages' x·W_g orientation: W_g [h'][E].
+ *  - dtype MOE_BF16: x, W_g, W_gate, W_up, W_down, x_packed, y_packed and y are bf16 (uint16
+ *    storage); accumulation is fp32. dtype MOE_F32: all of those are fp32. Biases, logits, gates
+ *    and the aux loss are fp32 in both.
+ *  - Thread safety: the library keeps no per-call state; concurrent calls need separate workspaces.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* a config field or pointer is invalid; nothing was enqueued     */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid for the method but not for this build (e.g. E > 256)     */
+  MOE_ERR_WORKSPACE = 3,     /* ws is NULL or not 256-byte aligned                             */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed                     */
+  MOE_ERR_DEVICE_STATUS = 5, /* a kernel found bad data (index/offsets out of range)            */
+  MOE_ERR_TIMEOUT = 6        /* a kernel wait gave up after its time limit                      */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+
+/* Softmax: TopK ranks the logits, gates = softmax over the K picked logits.
+ * Sigmoid: TopK ranks σ(l) + select_bias (formed in fp64), gates = σ(l_i) / Σ_picked σ(l_j). */
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
+
+typedef struct {
+  int64_t T;               /* tokens (>= 0)                                                      */
+  int32_t h;               /* token width, all heads                                             */
+  int32_t E;               /* experts, 1..256                                                    */
+  int32_t K;               /* experts per unit, 1..min(E, 8)                                     */
+  int32_t d_ff;            /* expert hidden width                                                */
+  int32_t n_heads;         /* H >= 1; H > 1 routes T·H sub-tokens of width h/H                  */
+  int32_t n_groups;        /* expert groups for the group limit (1 = off), E % n_groups == 0     */
+  int32_t topk_groups;     /* groups a unit may use (1..n_groups)                                */
+  float capacity_factor;   /* CF; <= 0 or +inf = no drop                                         */
+  float aux_alpha;         /* α of the aux loss (0.01 in the pages' HAI-LLM config)              */
+  int32_t score;           /* moe_score_t                                                        */
+  int32_t dtype;           /* moe_dtype_t                                                        */
+} moe_config_t;
+
+/* Weights of one layer (device pointers). logit_bias / select_bias may be NULL. */
+typedef struct {
+  const void* w_router;    /* W_g [h'][E]                                                        */
+  const float* logit_bias; /* [E] added to the logits (affects selection, gates and P_i)         */
+  const float* select_bias;/* [E] sigmoid scoring only: added to σ(l) for selection alone        */
+  const void* w_gate;      /* W1 [E][d_ff][h']                                                   */
+  const void* w_up;        /* W3 [E][d_ff][h']                                                   */
+  const void* w_down;      /* W2 [E][h'][d_ff]                                                   */
+} moe_weights_t;
+
+/* Optional outputs of moe_forward (device pointers; each may be NULL). */
+typedef struct {
+  int32_t* topk_idx;       /* [T'][K] picked experts, descending key, ties to the lower index    */
+  float* topk_gate;        /* [T'][K] gates                                                      */
+  float* logits;           /* [T'][E] fp32 router logits (logit bias included)                   */
+  int32_t* counts;         /* [E] pre-drop picks per expert                                      */
+  int32_t* offsets;        /* [E+1] exclusive scan of kept rows per expert                       */
+  int32_t* slot_of;        /* [T'][K] packed row of pick (t,k), -1 if dropped                    */
+  float* aux;              /* [1] aux loss                                                       */
+} moe_outputs_t;
+
+/* Bytes of workspace the calls need for this config (host only; no GPU call). Returns 0 for an
+ * invalid config. One workspace serves every call below for the same config. */
+MOE_API size_t moe_workspace_size(const moe_config_t* cfg);
+
+/* Zero the workspace's status header. Call once after allocating `ws`. Enqueued on `stream`. */
+MOE_API moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, moe_stream_t stream);
+
+/* Capacity C = ceil(CF·K·T'/E) (fp64 arithmetic from the fp32 CF), or -1 for no drop;
+ * -2 for an invalid config. [Lesson 10 §4] Host only. */
+MOE_API int64_t moe_capacity(const moe_config_t* cfg);
+
+/* Router + scoring + group limit + Top-K + gates (+ aux statistics).   [Lesson 10 §1, §4, §5]
+ *  x [T][h] (dtype), w_router [h'][E] (dtype), logit_bias/select_bias [E] fp32 or NULL.
+ *  Out: topk_idx [T'][K] int32, topk_gate [T'][K] fp32; logits_out [T'][E] fp32 or NULL;
+ *  aux_out [1] fp32 or NULL (uses the pre-drop counts of these picks). */
+MOE_API moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_router,
+                       const float* logit_bias, const float* select_bias, int32_t* topk_idx,
+                       float* topk_gate, float* logits_out, float* aux_out, void* ws,
+                       moe_stream_t stream);
+
+/* The same routing from given fp32 logits [T'][E] (no router GEMM): the logit bias, if any, is
+ * added in fp32 before selection.                                       [Lesson 10 §1, §4, §5] */
+MOE_API moe_status_t moe_route_logits(const moe_config_t* cfg, const float* logits, const float* logit_bias,
+                              const float* select_bias, int32_t* topk_idx, float* topk_gate,
+                              float* aux_out, void* ws, moe_stream_t stream);
+
+/* Capacity drop + pack.                                                 [Lesson 10 §3 step 1, §4]
+ *  topk_idx [T'][K] (each unit's K picks distinct, in [0,E)).
+ *  Out: counts [E] pre-drop picks (or NULL); offsets [E+1] kept rows per expert, exclusive scan;
+ *  slot_of [T'][K] packed row or -1 (dropped); row_token [T'·K] source unit of each packed row,
+ *  -1 past offsets[E]; x_packed [T'·K][h'] rows of x in packed order (rows past offsets[E] are
+ *  left untouched). Within an expert, rows are in unit order; pick (t,k) is dropped when t is at
+ *  or past place C of its expert's queue. */
+MOE_API moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
+                          int32_t* counts, int32_t* offsets, int32_t* slot_of, int32_t* row_token,
+                          void* x_packed, void* ws, moe_stream_t stream);
+
+/* Per-expert SwiGLU FFN over the packed rows (grouped GEMMs).           [Lesson 10 §3 step 2]
+ *  x_packed [T'·K][h'], offsets [E+1] (device; offsets[0] == 0, non-decreasing,
+ *  offsets[E] <= T'·K), w_gate/w_up [E][d_ff][h'], w_down [E][h'][d_ff].
+ *  Out: y_packed [T'·K][h'] rows [offsets[e], offsets[e+1]) = FFN_e of the same rows of x_packed;
+ *  rows past offsets[E] untouched. bf16: the hidden activation is rounded to bf16 once. */
+MOE_API moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_packed, const int32_t* offsets,
+                            const void* w_gate, const void* w_up, const void* w_down,
+                            void* y_packed, void* ws, moe_stream_t stream);
+
+/* Gate-weighted combine back to unit order.                             [Lesson 10 §1, §3 step 4]
+ *  y[u] = Σ_k topk_gate[u][k]·y_packed[slot_of[u][k]] over k with slot_of >= 0, in k order,
+ *  fp32 accumulation; y [T][h] (dtype; a unit with every pick dropped gets 0). */
+MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const void* y_packed, const int32_t* slot_of,
+                         const float* topk_gate, void* y, void* ws, moe_stream_t stream);
+
+/* The whole layer: route → dispatch → expert FFN → combine (+ aux). x [T][h] → y [T][h].
+ * `out` may be NULL or have NULL members; intermediates live in `ws`. */
+MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
+                         const moe_outputs_t* out, void* ws, moe_stream_t stream);
+
+/* Wait for `stream`, read and clear the status word in `ws`: MOE_OK, MOE_ERR_DEVICE_STATUS or
+ * MOE_ERR_TIMEOUT (or MOE_ERR_CUDA if the wait itself failed). */
+MOE_API moe_status_t moe_get_status(void* ws, moe_stream_t stream);
+
+/* Static text of a status code. */
+MOE_API const char* moe_status_string(moe_status_t s);
+
+/* Kernels this library has launched in this process (monotonic counter; host only). */
+MOE_API uint64_t moe_launch_count(void);
+
+/* MOE_ABI_VERSION of the loaded library. */
+MOE_API int32_t moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

@@ -1,0 +1,295 @@
+// The C ABI (include/moe.h): argument validation, workspace layout, and the order of the
+// kernel groups of each call. No allocation, no synchronisation except in moe_get_status.
+#include <math.h>
+#include <string.h>
+
+#include <atomic>
+#include <climits>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+int route_block_units(int E);  // route.cu
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                         uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || (reinterpret_cast<uintptr_t>(base) & 15) != 0 || (inner * 2) % 16 != 0) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+moe_status_t make_problem(const moe_config_t* c, Problem* p) {
+  if (!c || !p) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->h < 1 || c->n_heads < 1 || c->h % c->n_heads != 0) return MOE_ERR_INVALID_ARG;
+  if (c->E < 1 || c->K < 1 || c->K > c->E || c->d_ff < 1) return MOE_ERR_INVALID_ARG;
+  if (c->n_groups < 1 || c->E % c->n_groups != 0 || c->topk_groups < 1 || c->topk_groups > c->n_groups)
+    return MOE_ERR_INVALID_ARG;
+  if ((int64_t)c->K > (int64_t)c->topk_groups * (c->E / c->n_groups)) return MOE_ERR_INVALID_ARG;
+  if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (!isfinite(c->aux_alpha) || isnan(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+  if (c->E > kMaxExperts || c->K > kMaxTopK || c->n_groups > kMaxGroups) return MOE_ERR_UNSUPPORTED;
+  const int64_t Tu = c->T * (int64_t)c->n_heads;
+  const int hu = c->h / c->n_heads;
+  if (Tu > (int64_t)INT_MAX / 8 || Tu * c->K > (int64_t)INT_MAX) return MOE_ERR_UNSUPPORTED;
+  const bool bf16 = c->dtype == MOE_BF16;
+  if (bf16 && (hu % 32 != 0 || c->d_ff % 32 != 0)) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->E * (bf16 ? c->d_ff : 1) > (int64_t)INT_MAX || (int64_t)c->E * hu > (int64_t)INT_MAX)
+    return MOE_ERR_UNSUPPORTED;
+  p->cfg = *c;
+  p->Tu = Tu;
+  p->hu = hu;
+  p->E = c->E;
+  p->K = c->K;
+  p->d_ff = c->d_ff;
+  p->n_groups = c->n_groups;
+  p->topk_groups = c->topk_groups;
+  p->bf16 = bf16;
+  p->sigmoid = c->score == MOE_SCORE_SIGMOID;
+  const double cf = (double)c->capacity_factor;
+  if (!(cf > 0.0) || isinf(cf)) p->C = INT64_MAX;
+  else p->C = (int64_t)ceil(cf * (double)c->K * (double)Tu / (double)c->E);
+  p->rows = Tu * c->K;
+  p->nchunks = (Tu + kChunk - 1) / kChunk;
+  p->route_bt = route_block_units(c->E);
+  p->route_blocks = (Tu + p->route_bt - 1) / p->route_bt;
+  p->elt = bf16 ? 2 : 4;
+  return MOE_OK;
+}
+
+WsLayout ws_layout(const Problem& p) {
+  WsLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += (bytes + kWsAlign - 1) / kWsAlign * kWsAlign;
+    return at;
+  };
+  const size_t E = (size_t)p.E, TK = (size_t)p.Tu * p.K, rows = (size_t)p.rows;
+  L.status = take(kWsAlign);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.chunk_hist = take((size_t)p.nchunks * E * 4);
+  L.chunk_base = take((size_t)p.nchunks * E * 4);
+  L.psum_part = take((size_t)p.route_blocks * E * 4);
+  L.cnt_part = take((size_t)p.route_blocks * E * 4);
+  L.idx = take(TK * 4);
+  L.gate = take(TK * 4);
+  L.slot_of = take(TK * 4);
+  L.row_token = take(rows * 4);
+  L.x_packed = take(rows * (size_t)p.hu * p.elt);
+  L.hidden = take(rows * (size_t)p.d_ff * p.elt);
+  L.y_packed = take(rows * (size_t)p.hu * p.elt);
+  L.total = off;
+  return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+static bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; }
+static bool ws_ok(const void* ws) { return ws && (reinterpret_cast<uintptr_t>(ws) & 255) == 0; }
+static moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace missing or misaligned";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_STATUS: return "kernel found invalid data";
+    case MOE_ERR_TIMEOUT: return "kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t moe_workspace_size(const moe_config_t* cfg) {
+  Problem p;
+  if (make_problem(cfg, &p) != MOE_OK) return 0;
+  return ws_layout(p).total;
+}
+
+int64_t moe_capacity(const moe_config_t* cfg) {
+  Problem p;
+  if (make_problem(cfg, &p) != MOE_OK) return -2;
+  return p.C == INT64_MAX ? -1 : p.C;
+}
+
+moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, moe_stream_t stream) {
+  Problem p;
+  const moe_status_t st = make_problem(cfg, &p);
+  if (st != MOE_OK) return st;
+  if (!ws_ok(ws)) return MOE_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, kWsAlign, (cudaStream_t)stream));
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_router,
+                       const float* logit_bias, const float* select_bias, int32_t* topk_idx,
+                       float* topk_gate, float* logits_out, float* aux_out, void* ws,
+                       moe_stream_t stream) {
+  Problem p;
+  const moe_status_t st = make_problem(cfg, &p);
+  if (st != MOE_OK) return st;
+  if (!ws_ok(ws)) return MOE_ERR_WORKSPACE;
+  if (p.Tu > 0 && (!x || !w_router || !topk_idx || !topk_gate)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_route(p, x, w_router, nullptr, logit_bias, select_bias, topk_idx,
+                                  topk_gate, logits_out, aux_out, ws, (cudaStream_t)stream));
+}
+
+moe_status_t moe_route_logits(const moe_config_t* cfg, const float* logits, const float* logit_bias,
+                              const float* select_bias, int32_t* topk_idx, float* topk_gate,
+                              float* aux_out, void* ws, moe_stream_t stream) {
+  Problem p;
+  const moe_status_t st = make_problem(cfg, &p);
+  if (st != MOE_OK) return st;
+  if (!ws_ok(ws)) return MOE_ERR_WORKSPACE;
+  if (p.Tu > 0 && (!logits || !topk_idx || !topk_gate)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_route(p, nullptr, nullptr, logits, logit_bias, select_bias, topk_idx,
+                                  topk_gate, nullptr, aux_out, ws, (cudaStream_t)stream));
+}
+
+moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
+                          int32_t* counts, int32_t* offsets, int32_t* slot_of, int32_t* row_token,
+                          void* x_packed, void* ws, moe_stream_t stream) {
+  Problem p;
+  const moe_status_t st = make_problem(cfg, &p);
+  if (st != MOE_OK) return st;
+  if (!ws_ok(ws)) return MOE_ERR_WORKSPACE;
+  if (!offsets) return MOE_ERR_INVALID_ARG;
+  if (p.Tu > 0 && (!x || !topk_idx || !slot_of || !row_token || !x_packed)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_dispatch(p, x, topk_idx, counts, offsets, slot_of, row_token, x_packed,
+                                     ws, (cudaStream_t)stream));
+}
+
+moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_packed, const int32_t* offsets,
+                            const void* w_gate, const void* w_up, const void* w_down,
+                            void* y_packed, void* ws, moe_stream_t stream) {
+  Problem p;
+  const moe_status_t st = make_problem(cfg, &p);
+  if (st != MOE_OK) return st;
+  if (!ws_ok(ws)) return MOE_ERR_WORKSPACE;
+  if (!offsets || !w_gate || !w_up || !w_down) return MOE_ERR_INVALID_ARG;
+  if (p.rows > 0 && (!x_packed || !y_packed)) return MOE_ERR_INVALID_ARG;
+  if (p.bf16 && !(aligned16(x_packed) && aligned16(w_gate) && aligned16(w_up) && aligned16(w_down) &&
+                  aligned16(y_packed)))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(p);
+  return cuda_status(launch_expert_ffn(p, x_packed, offsets, w_gate, w_up, w_down,
+                                       ws_ptr<void>(ws, L.hidden), y_packed,
+                                       ws_ptr<uint32_t>(ws, L.status), (cudaStream_t)stream));
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* y_packed, const int32_t* slot_of,
+                         const float* topk_gate, void* y, void* ws, moe_stream_t stream) {
+  Problem p;
+  const moe_status_t st = make_problem(cfg, &p);
+  if (st != MOE_OK) return st;
+  if (!ws_ok(ws)) return MOE_ERR_WORKSPACE;
+  if (p.Tu > 0 && (!y_packed || !slot_of || !topk_gate || !y)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(p);
+  return cuda_status(launch_combine(p, y_packed, slot_of, topk_gate, y,
+                                    ws_ptr<uint32_t>(ws, L.status), (cudaStream_t)stream));
+}
+
+moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
+                         const moe_outputs_t* out, void* ws, moe_stream_t stream) {
+  Problem p;
+  const moe_status_t st = make_problem(cfg, &p);
+  if (st != MOE_OK) return st;
+  if (!ws_ok(ws)) return MOE_ERR_WORKSPACE;
+  if (!w || !w->w_router || !w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
+  if (p.Tu > 0 && (!x || !y)) return MOE_ERR_INVALID_ARG;
+  if (p.bf16 && !(aligned16(w->w_gate) && aligned16(w->w_up) && aligned16(w->w_down)))
+    return MOE_ERR_INVALID_ARG;
+  moe_outputs_t none;
+  memset(&none, 0, sizeof(none));
+  const moe_outputs_t& o = out ? *out : none;
+  const WsLayout L = ws_layout(p);
+  const cudaStream_t s = (cudaStream_t)stream;
+  int32_t* idx = o.topk_idx ? o.topk_idx : ws_ptr<int32_t>(ws, L.idx);
+  float* gate = o.topk_gate ? o.topk_gate : ws_ptr<float>(ws, L.gate);
+  int32_t* slot_of = o.slot_of ? o.slot_of : ws_ptr<int32_t>(ws, L.slot_of);
+  int32_t* row_token = ws_ptr<int32_t>(ws, L.row_token);
+  int32_t* offsets_ws = ws_ptr<int32_t>(ws, L.offsets);
+  void* x_packed = ws_ptr<void>(ws, L.x_packed);
+  void* hidden = ws_ptr<void>(ws, L.hidden);
+  void* y_packed = ws_ptr<void>(ws, L.y_packed);
+  uint32_t* status = ws_ptr<uint32_t>(ws, L.status);
+
+  cudaError_t e = launch_route(p, x, w->w_router, nullptr, w->logit_bias, w->select_bias, idx, gate,
+                               o.logits, o.aux, ws, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  // the scan writes the offsets into the workspace; the caller's copy is optional
+  e = launch_dispatch(p, x, idx, o.counts, o.offsets ? o.offsets : offsets_ws, slot_of, row_token,
+                      x_packed, ws, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_expert_ffn(p, x_packed, offsets_ws, w->w_gate, w->w_up, w->w_down, hidden, y_packed,
+                        status, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_combine(p, y_packed, slot_of, gate, y, status, s);
+  return cuda_status(e);
+}
+
+moe_status_t moe_get_status(void* ws, moe_stream_t stream) {
+  if (!ws_ok(ws)) return MOE_ERR_WORKSPACE;
+  uint32_t word = 0;
+  const cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (word != 0) {
+    if (cudaMemsetAsync(ws, 0, sizeof(word), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (word & kDevErrTimeout) return MOE_ERR_TIMEOUT;
+  return word ? MOE_ERR_DEVICE_STATUS : MOE_OK;
+}
+
+}  // extern "C"

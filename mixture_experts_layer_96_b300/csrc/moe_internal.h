@@ -1,0 +1,91 @@
+// Host-side internals of the C ABI: validated problem description, workspace layout and the
+// launchers of each kernel group. Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+constexpr int kMaxGroups = 32;
+constexpr int kChunk = 256;          // units per dispatch chunk (one block, one thread per unit)
+constexpr size_t kWsAlign = 1024;
+
+// A validated configuration with the derived sizes every launcher needs.
+struct Problem {
+  moe_config_t cfg;
+  int64_t Tu;        // routed units T' = T·H
+  int hu;            // unit width h' = h/H
+  int E, K, d_ff;
+  int n_groups, topk_groups;
+  bool bf16;
+  bool sigmoid;
+  int64_t C;         // capacity, or INT64_MAX for no drop
+  int64_t rows;      // packed-row capacity T'·K
+  int64_t nchunks;   // ceil(T'/kChunk)
+  int route_bt;      // units per router block
+  int64_t route_blocks;
+  size_t elt;        // bytes per activation/weight element (2 or 4)
+};
+
+// Offsets (bytes) of the workspace regions; every region starts 1024-byte aligned.
+struct WsLayout {
+  size_t status;       // uint32 status word + aux finalize ticket
+  size_t counts;       // int32 [E]
+  size_t offsets;      // int32 [E+1]
+  size_t chunk_hist;   // int32 [nchunks][E]
+  size_t chunk_base;   // int32 [nchunks][E]
+  size_t psum_part;    // float [route_blocks][E]
+  size_t cnt_part;     // int32 [route_blocks][E]
+  size_t idx;          // int32 [T'][K]
+  size_t gate;         // float [T'][K]
+  size_t slot_of;      // int32 [T'][K]
+  size_t row_token;    // int32 [T'K]
+  size_t x_packed;     // elt [T'K][h']
+  size_t hidden;       // elt [T'K][d_ff]
+  size_t y_packed;     // elt [T'K][h']
+  size_t total;
+};
+
+moe_status_t make_problem(const moe_config_t* cfg, Problem* p);
+WsLayout ws_layout(const Problem& p);
+
+template <typename T>
+inline T* ws_ptr(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// Per-device facts (cached).
+int device_sm_count();
+
+// Counts every kernel this library enqueues.
+void note_launch(int n = 1);
+
+// Tensor-map encoding through the driver entry point (no link-time libcuda dependency).
+bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                         uint32_t box_inner, uint32_t box_outer);
+
+// ---- launchers (return cudaSuccess or the launch error) --------------------------------------
+cudaError_t launch_route(const Problem& p, const void* x, const void* w_router,
+                         const float* logits_in, const float* logit_bias, const float* select_bias,
+                         int32_t* idx, float* gate, float* logits_out, float* aux_out, void* ws,
+                         cudaStream_t s);
+
+cudaError_t launch_dispatch(const Problem& p, const void* x, const int32_t* idx, int32_t* counts,
+                            int32_t* offsets, int32_t* slot_of, int32_t* row_token, void* x_packed,
+                            void* ws, cudaStream_t s);
+
+cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int32_t* offsets,
+                              const void* w_gate, const void* w_up, const void* w_down,
+                              void* hidden, void* y_packed, uint32_t* status, cudaStream_t s);
+
+cudaError_t launch_combine(const Problem& p, const void* y_packed, const int32_t* slot_of,
+                           const float* gate, void* y, uint32_t* status, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,360 @@
+"""Python binding of the C ABI in include/moe.h (argument marshalling only).
+
+Every compute step runs in the CUDA library `libmoe.so`; this module only checks tensor shapes,
+dtypes and devices, passes raw device pointers and the current CUDA stream, and turns status codes
+into exceptions. It has no fallback: if the library is missing it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
+MOE_ERR_CUDA, MOE_ERR_DEVICE_STATUS, MOE_ERR_TIMEOUT = 4, 5, 6
+MOE_F32, MOE_BF16 = 0, 1
+MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
+
+EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_capacity", "moe_route", "moe_route_logits",
+           "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_status",
+           "moe_status_string", "moe_launch_count", "moe_abi_version")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+
+
+class MoEConfig(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("h", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
+                ("capacity_factor", ctypes.c_float), ("aux_alpha", ctypes.c_float),
+                ("score", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+    @property
+    def T_units(self) -> int:
+        return self.T * self.n_heads
+
+    @property
+    def h_unit(self) -> int:
+        return self.h // self.n_heads
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == MOE_BF16 else torch.float32
+
+
+class MoEWeights(ctypes.Structure):
+    _fields_ = [("w_router", ctypes.c_void_p), ("logit_bias", ctypes.c_void_p),
+                ("select_bias", ctypes.c_void_p), ("w_gate", ctypes.c_void_p),
+                ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p)]
+
+
+class MoEOutputs(ctypes.Structure):
+    _fields_ = [("topk_idx", ctypes.c_void_p), ("topk_gate", ctypes.c_void_p),
+                ("logits", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("slot_of", ctypes.c_void_p), ("aux", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmoe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m mixture_experts_layer_96_b300.build`")
+    lib = ctypes.CDLL(path)
+    P, S, I32, I64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64
+    cfgp = ctypes.POINTER(MoEConfig)
+    sig = {
+        "moe_workspace_size": (S, [cfgp]),
+        "moe_workspace_init": (I32, [cfgp, P, P]),
+        "moe_capacity": (I64, [cfgp]),
+        "moe_route": (I32, [cfgp, P, P, P, P, P, P, P, P, P, P]),
+        "moe_route_logits": (I32, [cfgp, P, P, P, P, P, P, P, P]),
+        "moe_dispatch": (I32, [cfgp, P, P, P, P, P, P, P, P, P]),
+        "moe_expert_ffn": (I32, [cfgp, P, P, P, P, P, P, P, P]),
+        "moe_combine": (I32, [cfgp, P, P, P, P, P, P]),
+        "moe_forward": (I32, [cfgp, P, ctypes.POINTER(MoEWeights), P, ctypes.POINTER(MoEOutputs), P, P]),
+        "moe_get_status": (I32, [P, P]),
+        "moe_status_string": (ctypes.c_char_p, [I32]),
+        "moe_launch_count": (ctypes.c_uint64, []),
+        "moe_abi_version": (I32, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().moe_status_string(code).decode()
+
+
+def make_config(T: int, h: int, E: int, K: int, d_ff: int, *, n_heads: int = 1, n_groups: int = 1,
+                topk_groups: int = 1, capacity_factor: Optional[float] = None, aux_alpha: float = 0.01,
+                score: str = "softmax", dtype: str = "bf16") -> MoEConfig:
+    cf = 0.0 if capacity_factor is None or math.isinf(capacity_factor) else float(capacity_factor)
+    return MoEConfig(T, h, E, K, d_ff, n_heads, n_groups, topk_groups, cf, aux_alpha,
+                     MOE_SCORE_SIGMOID if score == "sigmoid" else MOE_SCORE_SOFTMAX,
+                     MOE_BF16 if dtype == "bf16" else MOE_F32)
+
+
+def workspace_size(cfg: MoEConfig) -> int:
+    n = load_library().moe_workspace_size(ctypes.byref(cfg))
+    if n == 0:
+        raise MoEError(MOE_ERR_INVALID_ARG, "moe_workspace_size")
+    return n
+
+
+def capacity(cfg: MoEConfig) -> Optional[int]:
+    c = load_library().moe_capacity(ctypes.byref(cfg))
+    if c == -2:
+        raise MoEError(MOE_ERR_INVALID_ARG, "moe_capacity")
+    return None if c == -1 else int(c)
+
+
+def launch_count() -> int:
+    return int(load_library().moe_launch_count())
+
+
+# ------------------------------------------------------------------------------------------------
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _check(code: int, where: str):
+    if code != MOE_OK:
+        raise MoEError(code, where)
+
+
+def _req(t: torch.Tensor, name: str, shape, dtype, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype} != {dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+class Workspace:
+    """Device scratch of one config (a torch uint8 tensor), status header zeroed at creation."""
+
+    def __init__(self, cfg: MoEConfig, device="cuda", stream=None):
+        self.cfg = cfg
+        self.nbytes = workspace_size(cfg)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        assert self.buf.data_ptr() % 1024 == 0 or self.buf.data_ptr() % 256 == 0
+        _check(load_library().moe_workspace_init(ctypes.byref(cfg), self.ptr, _stream(stream)),
+               "moe_workspace_init")
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def status(self, stream=None) -> int:
+        """Wait for the stream; read and clear the device status word."""
+        return int(load_library().moe_get_status(self.ptr, _stream(stream)))
+
+    def check(self, stream=None):
+        _check(self.status(stream), "moe_get_status")
+
+
+def moe_get_status(ws: Workspace, stream=None) -> int:
+    return ws.status(stream)
+
+
+def moe_route(cfg: MoEConfig, x, w_router, logit_bias=None, select_bias=None, *, ws: Workspace,
+              topk_idx=None, topk_gate=None, logits_out=None, aux_out=None, want_logits=False,
+              want_aux=False, stream=None):
+    """Router + scoring + Top-K + gates. Returns (topk_idx, topk_gate, logits or None, aux or None)."""
+    lib = load_library()
+    dt, dev = cfg.torch_dtype, x.device
+    Tu, hu, E, K = cfg.T_units, cfg.h_unit, cfg.E, cfg.K
+    _req(x, "x", (cfg.T, cfg.h), dt)
+    _req(w_router, "w_router", (hu, E), dt)
+    for b, n in ((logit_bias, "logit_bias"), (select_bias, "select_bias")):
+        if b is not None:
+            _req(b, n, (E,), torch.float32)
+    topk_idx = topk_idx if topk_idx is not None else torch.empty((Tu, K), dtype=torch.int32, device=dev)
+    topk_gate = topk_gate if topk_gate is not None else torch.empty((Tu, K), dtype=torch.float32, device=dev)
+    _req(topk_idx, "topk_idx", (Tu, K), torch.int32)
+    _req(topk_gate, "topk_gate", (Tu, K), torch.float32)
+    if logits_out is None and want_logits:
+        logits_out = torch.empty((Tu, E), dtype=torch.float32, device=dev)
+    if aux_out is None and want_aux:
+        aux_out = torch.empty((1,), dtype=torch.float32, device=dev)
+    _check(lib.moe_route(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(select_bias),
+                         _ptr(topk_idx), _ptr(topk_gate), _ptr(logits_out), _ptr(aux_out), ws.ptr,
+                         _stream(stream)), "moe_route")
+    return topk_idx, topk_gate, logits_out, aux_out
+
+
+def moe_route_logits(cfg: MoEConfig, logits, logit_bias=None, select_bias=None, *, ws: Workspace,
+                     topk_idx=None, topk_gate=None, aux_out=None, want_aux=False, stream=None):
+    """Routing from given fp32 logits [T'][E]. Returns (topk_idx, topk_gate, aux or None)."""
+    lib = load_library()
+    Tu, E, K, dev = cfg.T_units, cfg.E, cfg.K, logits.device
+    _req(logits, "logits", (Tu, E), torch.float32)
+    for b, n in ((logit_bias, "logit_bias"), (select_bias, "select_bias")):
+        if b is not None:
+            _req(b, n, (E,), torch.float32)
+    topk_idx = topk_idx if topk_idx is not None else torch.empty((Tu, K), dtype=torch.int32, device=dev)
+    topk_gate = topk_gate if topk_gate is not None else torch.empty((Tu, K), dtype=torch.float32, device=dev)
+    if aux_out is None and want_aux:
+        aux_out = torch.empty((1,), dtype=torch.float32, device=dev)
+    _check(lib.moe_route_logits(ctypes.byref(cfg), _ptr(logits), _ptr(logit_bias), _ptr(select_bias),
+                                _ptr(topk_idx), _ptr(topk_gate), _ptr(aux_out), ws.ptr, _stream(stream)),
+           "moe_route_logits")
+    return topk_idx, topk_gate, aux_out
+
+
+def moe_dispatch(cfg: MoEConfig, x, topk_idx, *, ws: Workspace, counts=None, offsets=None, slot_of=None,
+                 row_token=None, x_packed=None, stream=None):
+    """Capacity drop + pack. Returns (counts, offsets, slot_of, row_token, x_packed)."""
+    lib = load_library()
+    dt, dev = cfg.torch_dtype, x.device
+    Tu, hu, E, K = cfg.T_units, cfg.h_unit, cfg.E, cfg.K
+    _req(x, "x", (cfg.T, cfg.h), dt)
+    _req(topk_idx, "topk_idx", (Tu, K), torch.int32)
+    counts = counts if counts is not None else torch.empty((E,), dtype=torch.int32, device=dev)
+    offsets = offsets if offsets is not None else torch.empty((E + 1,), dtype=torch.int32, device=dev)
+    slot_of = slot_of if slot_of is not None else torch.empty((Tu, K), dtype=torch.int32, device=dev)
+    row_token = row_token if row_token is not None else torch.empty((Tu * K,), dtype=torch.int32, device=dev)
+    x_packed = x_packed if x_packed is not None else torch.empty((Tu * K, hu), dtype=dt, device=dev)
+    _req(counts, "counts", (E,), torch.int32)
+    _req(offsets, "offsets", (E + 1,), torch.int32)
+    _req(slot_of, "slot_of", (Tu, K), torch.int32)
+    _req(row_token, "row_token", (Tu * K,), torch.int32)
+    _req(x_packed, "x_packed", (Tu * K, hu), dt)
+    _check(lib.moe_dispatch(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts), _ptr(offsets),
+                            _ptr(slot_of), _ptr(row_token), _ptr(x_packed), ws.ptr, _stream(stream)),
+           "moe_dispatch")
+    return counts, offsets, slot_of, row_token, x_packed
+
+
+def moe_expert_ffn(cfg: MoEConfig, x_packed, offsets, w_gate, w_up, w_down, *, ws: Workspace,
+                   y_packed=None, stream=None):
+    """Per-expert SwiGLU FFN over packed rows. Returns y_packed [T'K][h']."""
+    lib = load_library()
+    dt, dev = cfg.torch_dtype, x_packed.device
+    Tu, hu, E, K, F = cfg.T_units, cfg.h_unit, cfg.E, cfg.K, cfg.d_ff
+    _req(x_packed, "x_packed", (Tu * K, hu), dt)
+    _req(offsets, "offsets", (E + 1,), torch.int32)
+    _req(w_gate, "w_gate", (E, F, hu), dt)
+    _req(w_up, "w_up", (E, F, hu), dt)
+    _req(w_down, "w_down", (E, hu, F), dt)
+    y_packed = y_packed if y_packed is not None else torch.empty((Tu * K, hu), dtype=dt, device=dev)
+    _req(y_packed, "y_packed", (Tu * K, hu), dt)
+    _check(lib.moe_expert_ffn(ctypes.byref(cfg), _ptr(x_packed), _ptr(offsets), _ptr(w_gate), _ptr(w_up),
+                              _ptr(w_down), _ptr(y_packed), ws.ptr, _stream(stream)), "moe_expert_ffn")
+    return y_packed
+
+
+def moe_combine(cfg: MoEConfig, y_packed, slot_of, topk_gate, *, ws: Workspace, y=None, stream=None):
+    """Gate-weighted combine back to unit order. Returns y [T][h]."""
+    lib = load_library()
+    dt, dev = cfg.torch_dtype, y_packed.device
+    Tu, hu, K = cfg.T_units, cfg.h_unit, cfg.K
+    _req(y_packed, "y_packed", (Tu * K, hu), dt)
+    _req(slot_of, "slot_of", (Tu, K), torch.int32)
+    _req(topk_gate, "topk_gate", (Tu, K), torch.float32)
+    y = y if y is not None else torch.empty((cfg.T, cfg.h), dtype=dt, device=dev)
+    _req(y, "y", (cfg.T, cfg.h), dt)
+    _check(lib.moe_combine(ctypes.byref(cfg), _ptr(y_packed), _ptr(slot_of), _ptr(topk_gate), _ptr(y),
+                           ws.ptr, _stream(stream)), "moe_combine")
+    return y
+
+
+@dataclass
+class LayerWeights:
+    """Device tensors of one layer."""
+    w_router: torch.Tensor
+    w_gate: torch.Tensor
+    w_up: torch.Tensor
+    w_down: torch.Tensor
+    logit_bias: Optional[torch.Tensor] = None
+    select_bias: Optional[torch.Tensor] = None
+
+    def check(self, cfg: MoEConfig):
+        dt, hu, E, F = cfg.torch_dtype, cfg.h_unit, cfg.E, cfg.d_ff
+        _req(self.w_router, "w_router", (hu, E), dt)
+        _req(self.w_gate, "w_gate", (E, F, hu), dt)
+        _req(self.w_up, "w_up", (E, F, hu), dt)
+        _req(self.w_down, "w_down", (E, hu, F), dt)
+        for b, n in ((self.logit_bias, "logit_bias"), (self.select_bias, "select_bias")):
+            if b is not None:
+                _req(b, n, (E,), torch.float32)
+
+    def c_struct(self) -> MoEWeights:
+        return MoEWeights(_ptr(self.w_router), _ptr(self.logit_bias), _ptr(self.select_bias),
+                          _ptr(self.w_gate), _ptr(self.w_up), _ptr(self.w_down))
+
+
+@dataclass
+class ForwardOutputs:
+    topk_idx: Optional[torch.Tensor] = None
+    topk_gate: Optional[torch.Tensor] = None
+    logits: Optional[torch.Tensor] = None
+    counts: Optional[torch.Tensor] = None
+    offsets: Optional[torch.Tensor] = None
+    slot_of: Optional[torch.Tensor] = None
+    aux: Optional[torch.Tensor] = None
+
+    @staticmethod
+    def allocate(cfg: MoEConfig, device, logits=True) -> "ForwardOutputs":
+        Tu, E, K = cfg.T_units, cfg.E, cfg.K
+        i32, f32 = torch.int32, torch.float32
+        return ForwardOutputs(
+            topk_idx=torch.empty((Tu, K), dtype=i32, device=device),
+            topk_gate=torch.empty((Tu, K), dtype=f32, device=device),
+            logits=torch.empty((Tu, E), dtype=f32, device=device) if logits else None,
+            counts=torch.empty((E,), dtype=i32, device=device),
+            offsets=torch.empty((E + 1,), dtype=i32, device=device),
+            slot_of=torch.empty((Tu, K), dtype=i32, device=device),
+            aux=torch.empty((1,), dtype=f32, device=device))
+
+    def c_struct(self) -> MoEOutputs:
+        return MoEOutputs(_ptr(self.topk_idx), _ptr(self.topk_gate), _ptr(self.logits), _ptr(self.counts),
+                          _ptr(self.offsets), _ptr(self.slot_of), _ptr(self.aux))
+
+
+def moe_forward(cfg: MoEConfig, x, weights: LayerWeights, *, ws: Workspace, y=None,
+                outputs: Optional[ForwardOutputs] = None, stream=None):
+    """The whole layer: x [T][h] → y [T][h]. `outputs` receives the optional intermediates."""
+    lib = load_library()
+    dt = cfg.torch_dtype
+    _req(x, "x", (cfg.T, cfg.h), dt)
+    weights.check(cfg)
+    y = y if y is not None else torch.empty((cfg.T, cfg.h), dtype=dt, device=x.device)
+    _req(y, "y", (cfg.T, cfg.h), dt)
+    cw = weights.c_struct()
+    co = outputs.c_struct() if outputs is not None else None
+    _check(lib.moe_forward(ctypes.byref(cfg), _ptr(x), ctypes.byref(cw), _ptr(y),
+                           ctypes.byref(co) if co is not None else None, ws.ptr, _stream(stream)),
+           "moe_forward")
+    return y

@@ -1,0 +1,84 @@
+"""The C-ABI library loads and exports every symbol include/moe.h declares; host-only calls and
+argument validation work without a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_layer_96_b300 import moe as M
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def declared_symbols():
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ("moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
+              "moe_workspace_size", "moe_get_status"):
+        assert n in names
+    assert set(names) == set(M.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = M.load_library()
+    for n in declared_symbols():
+        assert hasattr(lib, n), n
+    assert lib.moe_abi_version() == 1
+
+
+def _cfg(**kw):
+    base = dict(T=256, h=128, E=8, K=2, d_ff=256, capacity_factor=1.25, dtype="f32")
+    base.update(kw)
+    T, h, E, K, d_ff = (base.pop(k) for k in ("T", "h", "E", "K", "d_ff"))
+    return M.make_config(T, h, E, K, d_ff, **base)
+
+
+def test_capacity_host():
+    assert M.capacity(_cfg()) == 80
+    assert M.capacity(_cfg(T=16384, h=2048, E=64, K=2, d_ff=1408, dtype="bf16")) == 640
+    assert M.capacity(_cfg(capacity_factor=None)) is None
+    assert M.capacity(_cfg(T=4, n_heads=4, h=128, capacity_factor=1.0)) == 4  # T' = 16 units
+
+
+def test_workspace_size_host():
+    n = M.workspace_size(_cfg())
+    assert n > 0 and n % 1024 == 0
+    big = M.workspace_size(_cfg(T=4096, h=4096, E=8, K=2, d_ff=14336, dtype="bf16", capacity_factor=None))
+    # packed x, hidden and packed y for T'K = 8192 rows dominate
+    assert big >= 8192 * (4096 + 14336 + 4096) * 2
+
+
+@pytest.mark.parametrize("bad", [
+    dict(E=0), dict(K=3, E=2), dict(K=9, E=16), dict(E=257), dict(h=130, n_heads=4),
+    dict(n_groups=3), dict(n_groups=4, topk_groups=5), dict(n_groups=4, topk_groups=1, K=3),
+    dict(dtype="bf16", h=100), dict(d_ff=0), dict(T=-1),
+])
+def test_invalid_configs_rejected_on_host(bad):
+    cfg = _cfg(**bad)
+    lib = M.load_library()
+    assert lib.moe_workspace_size(ctypes.byref(cfg)) == 0
+    code = lib.moe_forward(ctypes.byref(cfg), None, None, None, None, None, None)
+    assert code in (M.MOE_ERR_INVALID_ARG, M.MOE_ERR_UNSUPPORTED)
+
+
+def test_missing_workspace_and_pointers_rejected():
+    lib = M.load_library()
+    cfg = _cfg()
+    w = M.MoEWeights()
+    assert lib.moe_forward(ctypes.byref(cfg), 16, ctypes.byref(w), 16, None, None, None) == M.MOE_ERR_WORKSPACE
+    assert lib.moe_forward(ctypes.byref(cfg), 16, ctypes.byref(w), 16, None, 4096, None) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(ctypes.byref(cfg), None, None, None, None, None, None, None, None, 4096, None) \
+        == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_get_status(None, None) == M.MOE_ERR_WORKSPACE
+    assert M.status_string(M.MOE_ERR_TIMEOUT) == "kernel wait timed out"
+
+
+def test_launch_counter_is_readable_on_host():
+    assert isinstance(M.launch_count(), int) and M.launch_count() >= 0

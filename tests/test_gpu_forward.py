@@ -1,0 +1,134 @@
+"""End-to-end parity of moe_forward against the oracle (GPU).
+
+The oracle routes on its own float64 logits. Where a unit's routing decision has a margin larger
+than the fp32 logits' error bound, the GPU must pick exactly the oracle's experts; inside the
+bound either choice is valid and is checked for validity. Given the (checked) routing, counts,
+offsets and packed slots must match the oracle bit-exactly, and y must meet the layer's float
+tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+from harness import Inputs, as_f64, bits_of, check_routing, config_of, tol_ok
+from mixture_experts_layer_96_b300 import (ForwardOutputs, Workspace, moe_combine, moe_dispatch,
+                                           moe_expert_ffn, moe_forward, moe_route)
+from workloads import WORKLOADS, MoEShape, scaled
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+
+
+SMALL = [
+    WORKLOADS["tiny_f32"],
+    scaled(WORKLOADS["mixtral_bf16"], T=700, h=512, d_ff=1024),
+    scaled(WORKLOADS["finegrained_bf16"], T=300, h=512, d_ff=256),
+    scaled(WORKLOADS["skewed_bf16"], T=3000, h=256, d_ff=384),
+    scaled(WORKLOADS["multihead_bf16"], T=600, h=1024, d_ff=512),
+    MoEShape("drop_heavy", T=500, h=128, E=4, K=2, d_ff=128, capacity_factor=0.3, logit_bias="zipf1.2"),
+    MoEShape("one_unit", T=1, h=64, E=8, K=2, d_ff=64),
+    MoEShape("dense_e1", T=200, h=64, E=1, K=1, d_ff=96),
+]
+
+
+def run_forward(inp: Inputs):
+    cfg = config_of(inp.shape)
+    x, lw = inp.device()
+    ws = Workspace(cfg)
+    outs = ForwardOutputs.allocate(cfg, "cuda")
+    y = moe_forward(cfg, x, lw, ws=ws, outputs=outs)
+    ws.check()
+    return y, outs
+
+
+def check_forward(inp: Inputs, y, outs, sample=None):
+    s = inp.shape
+    ref = inp.oracle_forward(sample_units=sample)
+    bound = inp.logit_error_bound()
+    gl = as_f64(outs.logits)
+    assert (np.abs(gl - ref.logits) <= bound).all(), float(np.max(np.abs(gl - ref.logits) - bound))
+    gidx = bits_of(outs.topk_idx).astype(np.int64)
+    key_err = bound if s.score == "softmax" else bound / 4.0  # σ is 1/4-Lipschitz
+    n_amb, n_diff = check_routing(gidx, ref.idx, ref.keys, key_err, s)
+    if n_diff:
+        ref = inp.oracle_forward(sample_units=sample, idx_override=gidx)
+    d = ref.dispatch
+    np.testing.assert_array_equal(bits_of(outs.counts), d.counts)
+    np.testing.assert_array_equal(bits_of(outs.offsets), d.offsets)
+    np.testing.assert_array_equal(bits_of(outs.slot_of), d.slot_of)
+    gate_tol = 2.0 * float(bound.max()) + 2e-6
+    np.testing.assert_allclose(as_f64(outs.topk_gate), ref.gate, atol=gate_tol, rtol=0)
+    aux = float(outs.aux.item())
+    assert abs(aux - ref.aux) <= 1e-4 * abs(ref.aux) + 1e-7, (aux, ref.aux)
+    yg = as_f64(y)
+    if sample is None:
+        ok, err, tb = tol_ok(yg, ref.y, s.dtype)
+    else:
+        yu = yg.reshape(s.T_units, s.h_unit)
+        got = np.stack([yu[u] for u in sample])
+        want = np.stack([ref.y_units[int(u)] for u in sample])
+        ok, err, tb = tol_ok(got, want, s.dtype)
+    assert ok, f"max |y - y_ref| = {err} > {tb}"
+    return n_amb, n_diff
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
+def test_forward_parity_small(shape):
+    inp = Inputs.make(shape)
+    y, outs = run_forward(inp)
+    check_forward(inp, y, outs)
+
+
+def test_forward_is_deterministic_and_equals_the_stages():
+    shape = scaled(WORKLOADS["skewed_bf16"], T=2000, h=256, d_ff=384)
+    inp = Inputs.make(shape)
+    cfg = config_of(shape)
+    x, lw = inp.device()
+    ws = Workspace(cfg)
+    y1 = moe_forward(cfg, x, lw, ws=ws)
+    y2 = moe_forward(cfg, x, lw, ws=ws)
+    ws.check()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    idx, gate, _, _ = moe_route(cfg, x, lw.w_router, lw.logit_bias, lw.select_bias, ws=ws)
+    counts, offsets, slot_of, row_token, xp = moe_dispatch(cfg, x, idx, ws=ws)
+    yp = moe_expert_ffn(cfg, xp, offsets, lw.w_gate, lw.w_up, lw.w_down, ws=ws)
+    y3 = moe_combine(cfg, yp, slot_of, gate, ws=ws)
+    ws.check()
+    assert torch.equal(y1.view(torch.int16), y3.view(torch.int16))
+
+
+def test_forward_empty_batch():
+    shape = MoEShape("empty", T=0, h=128, E=8, K=2, d_ff=128)
+    cfg = config_of(shape)
+    ws = Workspace(cfg)
+    inp = Inputs.make(scaled(shape, T=1))
+    _, lw = inp.device()
+    x = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
+    outs = ForwardOutputs.allocate(cfg, "cuda")
+    y = moe_forward(cfg, x, lw, ws=ws, outputs=outs)
+    ws.check()
+    assert y.shape == (0, 128)
+    assert bits_of(outs.counts).tolist() == [0] * 8
+    assert bits_of(outs.offsets).tolist() == [0] * 9
+    assert float(outs.aux.item()) == 0.0
+
+
+# ------------------------------------------------------------------------- full-size, sampled
+FULL = ["mixtral_bf16", "skewed_bf16", "multihead_bf16", "tiny_f32", "finegrained_bf16"]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", FULL)
+def test_forward_parity_full_size_sampled(name):
+    shape = WORKLOADS[name]
+    inp = Inputs.make(shape)
+    y, outs = run_forward(inp)
+    rng = np.random.default_rng(123)
+    n = 8 if shape.E >= 256 else 16
+    sample = np.sort(rng.choice(shape.T_units, size=min(n, shape.T_units), replace=False))
+    check_forward(inp, y, outs, sample=sample)
