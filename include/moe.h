@@ -75,6 +75,7 @@ typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
 
 typedef struct {
   int64_t T;               /* tokens (>= 0)                                                      */
+  double capacity_factor;  /* CF; <= 0 or +inf = no drop                                         */
   int32_t h;               /* token width, all heads                                             */
   int32_t E;               /* experts, 1..256                                                    */
   int32_t K;               /* experts per unit, 1..min(E, 8)                                     */
@@ -82,7 +83,6 @@ typedef struct {
   int32_t n_heads;         /* H >= 1; H > 1 routes T·H sub-tokens of width h/H                  */
   int32_t n_groups;        /* expert groups for the group limit (1 = off), E % n_groups == 0     */
   int32_t topk_groups;     /* groups a unit may use (1..n_groups)                                */
-  float capacity_factor;   /* CF; <= 0 or +inf = no drop                                         */
   float aux_alpha;         /* α of the aux loss (0.01 in the pages' HAI-LLM config)              */
   int32_t score;           /* moe_score_t                                                        */
   int32_t dtype;           /* moe_dtype_t                                                        */
@@ -116,7 +116,7 @@ MOE_API size_t moe_workspace_size(const moe_config_t* cfg);
 /* Zero the workspace's status header. Call once after allocating `ws`. Enqueued on `stream`. */
 MOE_API moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, moe_stream_t stream);
 
-/* Capacity C = ceil(CF·K·T'/E) (fp64 arithmetic from the fp32 CF), or -1 for no drop;
+/* Capacity C = ceil(CF·K·T'/E) evaluated in fp64 in that order, or -1 for no drop;
  * -2 for an invalid config. [Lesson 10 §4] Host only. */
 MOE_API int64_t moe_capacity(const moe_config_t* cfg);
 

@@ -86,7 +86,7 @@ moe_status_t make_problem(const moe_config_t* c, Problem* p) {
   p->topk_groups = c->topk_groups;
   p->bf16 = bf16;
   p->sigmoid = c->score == MOE_SCORE_SIGMOID;
-  const double cf = (double)c->capacity_factor;
+  const double cf = c->capacity_factor;
   if (!(cf > 0.0) || isinf(cf)) p->C = INT64_MAX;
   else p->C = (int64_t)ceil(cf * (double)c->K * (double)Tu / (double)c->E);
   p->rows = Tu * c->K;

@@ -34,11 +34,10 @@ class MoEError(RuntimeError):
 
 
 class MoEConfig(ctypes.Structure):
-    _fields_ = [("T", ctypes.c_int64), ("h", ctypes.c_int32), ("E", ctypes.c_int32),
-                ("K", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("n_heads", ctypes.c_int32),
-                ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
-                ("capacity_factor", ctypes.c_float), ("aux_alpha", ctypes.c_float),
-                ("score", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+    _fields_ = [("T", ctypes.c_int64), ("capacity_factor", ctypes.c_double), ("h", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("K", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("n_heads", ctypes.c_int32), ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
+                ("aux_alpha", ctypes.c_float), ("score", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
     @property
     def T_units(self) -> int:
@@ -109,9 +108,10 @@ def make_config(T: int, h: int, E: int, K: int, d_ff: int, *, n_heads: int = 1, 
                 topk_groups: int = 1, capacity_factor: Optional[float] = None, aux_alpha: float = 0.01,
                 score: str = "softmax", dtype: str = "bf16") -> MoEConfig:
     cf = 0.0 if capacity_factor is None or math.isinf(capacity_factor) else float(capacity_factor)
-    return MoEConfig(T, h, E, K, d_ff, n_heads, n_groups, topk_groups, cf, aux_alpha,
-                     MOE_SCORE_SIGMOID if score == "sigmoid" else MOE_SCORE_SOFTMAX,
-                     MOE_BF16 if dtype == "bf16" else MOE_F32)
+    return MoEConfig(T=T, capacity_factor=cf, h=h, E=E, K=K, d_ff=d_ff, n_heads=n_heads, n_groups=n_groups,
+                     topk_groups=topk_groups, aux_alpha=aux_alpha,
+                     score=MOE_SCORE_SIGMOID if score == "sigmoid" else MOE_SCORE_SOFTMAX,
+                     dtype=MOE_BF16 if dtype == "bf16" else MOE_F32)
 
 
 def workspace_size(cfg: MoEConfig) -> int:
