@@ -55,15 +55,19 @@ def dist_env():
 
 # ------------------------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 200 ms with host timestamps; summary() keeps the samples inside
+    a wall-clock window (the timed region), or, when that region is shorter than the sampling
+    period, the samples of the surrounding busy window (warm-up, timed loop, stage loop)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
+        self.lines = []
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
@@ -72,8 +76,7 @@ class ClockSampler:
             self.proc = None
         return self
 
-    def __exit__(self, *exc):
-        self.lines = []
+    def stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -83,24 +86,33 @@ class ClockSampler:
                 out, _ = self.proc.communicate()
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
-    def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
+    def _rows(self):
+        import datetime
+        rows = []
+        for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+        return rows
+
+    def summary(self, t0, t1, busy0, busy1):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = self._rows()
+        sel = [r for r in rows if t0 <= r[0] <= t1]
+        window = "timed region"
+        if not sel:
+            sel = [r for r in rows if busy0 <= r[0] <= busy1]
+            window = "busy window around the timed region (shorter than the 200 ms sampling period)"
+        if not sel:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        reasons = sorted({n for r in sel for n, v in zip(names, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": sel[-1][2], "reasons": reasons,
+                "samples": len(sel), "window": window}
 
 
 # ------------------------------------------------------------------------------------ inputs
@@ -253,8 +265,14 @@ def run_ours(args, shape):
             dist.barrier()
         torch.cuda.synchronize(device)
 
-    for _ in range(max(3, args.warmup)):
+    clk = ClockSampler(local).start()
+    busy0 = time.time()
+    n_warm = 0
+    while n_warm < max(3, args.warmup) or time.time() - busy0 < 1.0:
         moe_forward(cfg, x, lw, ws=ws, y=y, outputs=outs)
+        n_warm += 1
+        if n_warm % 50 == 0:
+            torch.cuda.synchronize(device)
     ws.check()
     kept = int(outs.offsets[-1].item())
     aux = float(outs.aux.item())
@@ -264,13 +282,14 @@ def run_ours(args, shape):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     n0 = launch_count()
-    with ClockSampler(local) as clk:
-        for i in range(args.steps):
-            flush.fill_(i & 0xFF)
-            ev[i][0].record(stream)
-            moe_forward(cfg, x, lw, ws=ws, y=y, outputs=outs)
-            ev[i][1].record(stream)
-        barrier()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        moe_forward(cfg, x, lw, ws=ws, y=y, outputs=outs)
+        ev[i][1].record(stream)
+    barrier()
+    t1 = time.time()
     n_launch = launch_count() - n0
     ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     if world > 1:
@@ -308,6 +327,9 @@ def run_ours(args, shape):
         for j, k in enumerate(st):
             st[k].append(e[j].elapsed_time(e[j + 1]))
     ws.check()
+    busy1 = time.time()
+    clk.stop()
+    clocks = clk.summary(t0, t1, busy0, busy1)
     stage_ms = {k: statistics.mean(v) for k, v in st.items()}
 
     # ---- e2e: pinned host x → device, forward, y → pinned host, every step
@@ -353,10 +375,9 @@ def run_ours(args, shape):
     stages["dispatch_frac_hbm"] = stages["dispatch_gbs"] / hbm
     stages["combine_frac_hbm"] = stages["combine_gbs"] / hbm
     value = world * shape.T / (ms * 1e-3)
-    clocks = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": n_warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if shape.dtype == "bf16" else "f32",
         "data": "synthetic (seeded generator; x~N(0,1), W~N(0,1/fan_in), bf16)",
         "config": {"workload": shape.describe(), "global_batch": shape.T * world, "units_per_gpu": shape.T_units,
@@ -385,7 +406,7 @@ def run_ours(args, shape):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral_bf16", choices=sorted(WORKLOADS))
