@@ -179,6 +179,30 @@ MOE_API uint64_t moe_launch_count(void);
 /* MOE_ABI_VERSION of the loaded library. */
 MOE_API int32_t moe_abi_version(void);
 
+/* Dispatch for callers that cannot allocate device memory. (The pages have no counterpart of this
+ * call; it exists for how the library is deployed, not for the method.)
+ * Some callers cannot call cudaMalloc: a plugin inside a host framework that owns all device
+ * memory and hands the plugin only its input and output buffers, or a serving process whose
+ * device memory is fixed at start-up and that allows no allocation afterwards. Such a caller
+ * cannot size and keep a workspace, so this call takes no `ws`: its scratch (per-chunk
+ * histograms and queue bases, per-expert totals and offsets) is a fixed 1 MiB array inside the
+ * library, which every GPU that loads the library holds until the process exits.
+ *  - Same inputs, outputs and results as moe_dispatch (bit for bit).
+ *  - Limit: 8·ceil(T'/256)·E bytes + about 8·E bytes must fit in 1 MiB (with E = 256, up to
+ *    about 130,000 units); larger problems return MOE_ERR_UNSUPPORTED and enqueue nothing.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
+ *    that device current) and keeps it; make that first call before any stream capture.
+ *  - It allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *  - All calls on a device share the array, which keeps the last call's contents; each call
+ *    rewrites every part it reads, so nothing needs clearing, but calls that overlap on the GPU
+ *    (e.g. on two streams) race and give wrong results. Serialise them.
+ *  - Bad indices (out of range or repeated within a unit) give that unit slot -1 for every pick,
+ *    as in moe_dispatch, but are not reported: there is no workspace status word here. */
+MOE_API moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const void* x,
+                                          const int32_t* topk_idx, int32_t* counts,
+                                          int32_t* offsets, int32_t* slot_of, int32_t* row_token,
+                                          void* x_packed, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,7 @@ MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_capacity", "moe_route", "moe_route_logits",
            "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_status",
-           "moe_status_string", "moe_launch_count", "moe_abi_version")
+           "moe_status_string", "moe_launch_count", "moe_abi_version", "moe_dispatch_noalloc")
 
 
 class MoEError(RuntimeError):
@@ -91,6 +91,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_status_string": (ctypes.c_char_p, [I32]),
         "moe_launch_count": (ctypes.c_uint64, []),
         "moe_abi_version": (I32, []),
+        "moe_dispatch_noalloc": (I32, [cfgp, P, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -358,3 +359,30 @@ def moe_forward(cfg: MoEConfig, x, weights: LayerWeights, *, ws: Workspace, y=No
                            ctypes.byref(co) if co is not None else None, ws.ptr, _stream(stream)),
            "moe_forward")
     return y
+
+
+NOALLOC_SCRATCH_BYTES = 1 << 20
+
+
+def moe_dispatch_noalloc(cfg: MoEConfig, x, topk_idx, *, counts=None, offsets=None, slot_of=None,
+                         row_token=None, x_packed=None, stream=None):
+    """moe_dispatch for callers that cannot allocate device memory: no workspace; the library's
+    fixed 1 MiB scratch array is used instead (calls that overlap on the GPU race).
+    Returns (counts, offsets, slot_of, row_token, x_packed)."""
+    lib = load_library()
+    dt, dev = cfg.torch_dtype, x.device
+    Tu, hu, E, K = cfg.T_units, cfg.h_unit, cfg.E, cfg.K
+    _req(x, "x", (cfg.T, cfg.h), dt)
+    _req(topk_idx, "topk_idx", (Tu, K), torch.int32)
+    counts = counts if counts is not None else torch.empty((E,), dtype=torch.int32, device=dev)
+    offsets = offsets if offsets is not None else torch.empty((E + 1,), dtype=torch.int32, device=dev)
+    slot_of = slot_of if slot_of is not None else torch.empty((Tu, K), dtype=torch.int32, device=dev)
+    row_token = row_token if row_token is not None else torch.empty((Tu * K,), dtype=torch.int32, device=dev)
+    x_packed = x_packed if x_packed is not None else torch.empty((Tu * K, hu), dtype=dt, device=dev)
+    code = lib.moe_dispatch_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts), _ptr(offsets),
+                                    _ptr(slot_of), _ptr(row_token), _ptr(x_packed), _stream(stream))
+    if code == MOE_ERR_UNSUPPORTED:
+        raise MoEError(code, f"moe_dispatch_noalloc: {Tu} units x {E} experts need more than the "
+                             f"{NOALLOC_SCRATCH_BYTES} bytes of fixed scratch")
+    _check(code, "moe_dispatch_noalloc")
+    return counts, offsets, slot_of, row_token, x_packed
