@@ -113,6 +113,14 @@ WsLayout ws_layout(const Problem& p) {
   L.chunk_base = take((size_t)p.nchunks * E * 4);
   L.psum_part = take((size_t)p.route_blocks * E * 4);
   L.cnt_part = take((size_t)p.route_blocks * E * 4);
+  L.aux_terms = take(E * 8);
+  if (p.bf16) {
+    const RouterPlan r = router_plan(p);
+    L.router_wt = take((size_t)r.N * p.hu * 2);
+    L.router_part = take((size_t)r.splits * (size_t)p.Tu * E * 4);
+  } else {
+    L.router_wt = L.router_part = off;
+  }
   L.idx = take(TK * 4);
   L.gate = take(TK * 4);
   L.slot_of = take(TK * 4);

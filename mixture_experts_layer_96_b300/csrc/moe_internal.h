@@ -16,6 +16,7 @@ constexpr int kMaxTopK = 8;
 constexpr int kMaxGroups = 32;
 constexpr int kChunk = 256;          // units per dispatch chunk (one block, one thread per unit)
 constexpr size_t kWsAlign = 1024;
+constexpr int kRouterSplitTarget = 160;  // aim for about this many router CTAs (>= SMs of a B300)
 
 // A validated configuration with the derived sizes every launcher needs.
 struct Problem {
@@ -34,15 +35,24 @@ struct Problem {
   size_t elt;        // bytes per activation/weight element (2 or 4)
 };
 
+// Tensor-core router GEMM plan: N = E rounded up to 16, K split into `splits` slices.
+struct RouterPlan {
+  int N, m_tiles, nkb, kb_per_split, splits;
+};
+RouterPlan router_plan(const Problem& p);
+
 // Offsets (bytes) of the workspace regions; every region starts 1024-byte aligned.
 struct WsLayout {
-  size_t status;       // uint32 status word + aux finalize ticket
+  size_t status;       // uint32 status word at +0, uint32 aux finalize ticket at +4
   size_t counts;       // int32 [E]
   size_t offsets;      // int32 [E+1]
   size_t chunk_hist;   // int32 [nchunks][E]
   size_t chunk_base;   // int32 [nchunks][E]
   size_t psum_part;    // float [route_blocks][E]
   size_t cnt_part;     // int32 [route_blocks][E]
+  size_t aux_terms;    // double [E] per-expert aux terms
+  size_t router_wt;    // bf16 [N][h'] transposed router weight (bf16 layers)
+  size_t router_part;  // float [splits][T'][E] partial logits (bf16 layers)
   size_t idx;          // int32 [T'][K]
   size_t gate;         // float [T'][K]
   size_t slot_of;      // int32 [T'][K]
@@ -76,6 +86,9 @@ cudaError_t launch_route(const Problem& p, const void* x, const void* w_router,
                          const float* logits_in, const float* logit_bias, const float* select_bias,
                          int32_t* idx, float* gate, float* logits_out, float* aux_out, void* ws,
                          cudaStream_t s);
+
+cudaError_t launch_router_tc(const Problem& p, const void* x, const void* w_router, void* wt, float* part,
+                             uint32_t* status, cudaStream_t s);
 
 cudaError_t launch_dispatch(const Problem& p, const void* x, const int32_t* idx, int32_t* counts,
                             int32_t* offsets, int32_t* slot_of, int32_t* row_token, void* x_packed,

@@ -44,7 +44,9 @@ struct RouteTile {
 struct RouteArgs {
   const void* x;            // [Tu][hu] (TIn)
   const void* w;            // [hu][E] (TIn)
-  const float* logits_in;   // [Tu][E] or null
+  const float* logits_in;   // [nparts][Tu][E] (summed in order) or null
+  int64_t part_stride;      // elements between parts
+  int nparts;
   const float* logit_bias;  // [E] or null
   const float* select_bias; // [E] or null
   int32_t* idx;             // [Tu][K]
@@ -89,6 +91,7 @@ route_kernel(RouteArgs a) {
       float v = 0.f;
       if (u < a.Tu && e < E) {
         v = a.logits_in[u * E + e];
+        for (int q = 1; q < a.nparts; ++q) v += a.logits_in[q * a.part_stride + u * E + e];
         if (a.logit_bias) v = v + a.logit_bias[e];
       }
       ls[r * (EP + 1) + e] = v;
@@ -350,29 +353,47 @@ route_kernel(RouteArgs a) {
   }
 }
 
-// aux = α·E·Σ_i (count_i/(T'·K))·(ΣP_i/T')  [Lesson 10 §4]; fixed-order fp64 reductions.
+// aux = α·E·Σ_i (count_i/(T'·K))·(ΣP_i/T')  [Lesson 10 §4]. One block per expert reduces that
+// expert's per-block partials (fixed strided order, then a fixed tree, in fp64); the last block
+// to finish (ticket counter) adds the E terms in expert order and resets the ticket.
 __global__ void __launch_bounds__(256)
 aux_finalize_kernel(const float* __restrict__ psum_part, const int32_t* __restrict__ cnt_part,
-                    int64_t blocks, int E, int64_t Tu, int K, float alpha, float* aux_out) {
-  __shared__ double red[256];
-  const int tid = threadIdx.x;
-  double term = 0.0;
-  if (tid < E && Tu > 0) {
-    double P = 0.0;
-    int64_t c = 0;
-    for (int64_t b = 0; b < blocks; ++b) {
-      P += (double)psum_part[b * E + tid];
-      c += cnt_part[b * E + tid];
-    }
-    term = ((double)c / ((double)Tu * K)) * (P / (double)Tu);
+                    int64_t blocks, int E, int64_t Tu, int K, float alpha, double* terms,
+                    unsigned int* ticket, float* aux_out) {
+  __shared__ double sP[256];
+  __shared__ long long sC[256];
+  __shared__ bool last;
+  const int tid = threadIdx.x, e = blockIdx.x;
+  double P = 0.0;
+  long long c = 0;
+  for (int64_t b = tid; b < blocks; b += 256) {
+    P += (double)psum_part[b * E + e];
+    c += cnt_part[b * E + e];
   }
-  red[tid] = term;
+  sP[tid] = P;
+  sC[tid] = c;
   __syncthreads();
   for (int s = 128; s; s >>= 1) {
-    if (tid < s) red[tid] += red[tid + s];
+    if (tid < s) {
+      sP[tid] += sP[tid + s];
+      sC[tid] += sC[tid + s];
+    }
     __syncthreads();
   }
-  if (tid == 0) *aux_out = (float)((double)alpha * E * red[0]);
+  if (tid == 0) {
+    terms[e] = Tu > 0 ? ((double)sC[0] / ((double)Tu * K)) * (sP[0] / (double)Tu) : 0.0;
+    __threadfence();
+    last = atomicAdd(ticket, 1u) == (unsigned)(E - 1);
+  }
+  __syncthreads();
+  if (last && tid == 0) {
+    __threadfence();
+    const volatile double* vt = terms;
+    double acc = 0.0;
+    for (int i = 0; i < E; ++i) acc += vt[i];
+    *aux_out = (float)((double)alpha * E * acc);
+    *ticket = 0u;
+  }
 }
 
 template <typename TIn, int EP, bool FL>
@@ -444,17 +465,32 @@ cudaError_t launch_route(const Problem& p, const void* x, const void* w_router,
   a.n_groups = p.n_groups;
   a.topk_groups = p.topk_groups;
   a.sigmoid = p.sigmoid ? 1 : 0;
+  a.part_stride = 0;
+  a.nparts = 1;
   const int64_t blocks = p.route_blocks;
   cudaError_t e = cudaSuccess;
   if (blocks > 0) {
-    if (logits_in) e = route_dispatch_ep<float, true>(p, a, blocks, s);
-    else if (p.bf16) e = route_dispatch_ep<__nv_bfloat16, false>(p, a, blocks, s);
-    else e = route_dispatch_ep<float, false>(p, a, blocks, s);
+    if (logits_in) {
+      e = route_dispatch_ep<float, true>(p, a, blocks, s);
+    } else if (p.bf16) {
+      // logits on the tensor cores, then the selection from the (split) fp32 logits
+      float* part = ws_ptr<float>(ws, L.router_part);
+      e = launch_router_tc(p, x, w_router, ws_ptr<void>(ws, L.router_wt), part,
+                           ws_ptr<uint32_t>(ws, L.status), s);
+      if (e != cudaSuccess) return e;
+      a.logits_in = part;
+      a.part_stride = p.Tu * p.E;
+      a.nparts = router_plan(p).splits;
+      e = route_dispatch_ep<float, true>(p, a, blocks, s);
+    } else {
+      e = route_dispatch_ep<float, false>(p, a, blocks, s);
+    }
     if (e != cudaSuccess) return e;
   }
   if (aux_out) {
-    aux_finalize_kernel<<<1, 256, 0, s>>>(a.psum_part, a.cnt_part, blocks, p.E, p.Tu, p.K,
-                                          p.cfg.aux_alpha, aux_out);
+    aux_finalize_kernel<<<p.E, 256, 0, s>>>(a.psum_part, a.cnt_part, blocks, p.E, p.Tu, p.K,
+                                            p.cfg.aux_alpha, ws_ptr<double>(ws, L.aux_terms),
+                                            ws_ptr<unsigned int>(ws, L.status + 4), aux_out);
     note_launch();
     e = cudaGetLastError();
   }

@@ -127,8 +127,15 @@ FFN_CASES = [
 ]
 
 
+@pytest.fixture(params=["single", "pair"])
+def tile_mode(request, monkeypatch):
+    """Run an expert-FFN case with the single-CTA 128-row tiles and with the CTA-pair 256-row tiles."""
+    monkeypatch.setenv("MOE_TC_PAIR", "1" if request.param == "pair" else "0")
+    return request.param
+
+
 @pytest.mark.parametrize("shape", FFN_CASES, ids=[s.name for s in FFN_CASES])
-def test_expert_ffn_parity(shape):
+def test_expert_ffn_parity(shape, tile_mode):
     cfg = config_of(shape)
     g = Generator(shape)
     b = shape.dtype == "bf16"
@@ -156,7 +163,7 @@ def test_expert_ffn_parity(shape):
     assert ok, f"max err {err} > {bound}"
 
 
-def test_expert_ffn_empty_and_skewed_experts():
+def test_expert_ffn_empty_and_skewed_experts(tile_mode):
     """Offsets with empty experts, one expert holding most rows, and unused rows at the end."""
     shape = MoEShape("skew_offsets", T=400, h=128, E=6, K=2, d_ff=256)
     cfg = config_of(shape)
