@@ -268,7 +268,7 @@ def run_ours(args, shape):
     clk = ClockSampler(local).start()
     busy0 = time.time()
     n_warm = 0
-    while n_warm < max(3, args.warmup) or time.time() - busy0 < 1.0:
+    while n_warm < max(3, args.warmup) or time.time() - busy0 < args.min_warmup_s:
         moe_forward(cfg, x, lw, ws=ws, y=y, outputs=outs)
         n_warm += 1
         if n_warm % 50 == 0:
@@ -413,6 +413,8 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=16, help="units the CPU-baseline oracle computes")
     ap.add_argument("--ref-sample", type=int, default=2, help="units per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-warmup-s", type=float, default=1.0,
+                    help="keep warming up at least this long (steady clocks); 0 for profiling runs")
     args = ap.parse_args()
     shape = WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -119,7 +119,8 @@ WsLayout ws_layout(const Problem& p) {
     L.router_wt = take((size_t)r.N * p.hu * 2);
     L.router_part = take((size_t)r.splits * (size_t)p.Tu * E * 4);
   } else {
-    L.router_wt = L.router_part = off;
+    L.router_wt = off;
+    L.router_part = take((size_t)p.Tu * E * 4);
   }
   L.idx = take(TK * 4);
   L.gate = take(TK * 4);

@@ -266,7 +266,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-z)); }
+// silu(z) = z·σ(z) for the bf16 epilogues: fast exp and division (a few ulp of fp32, far below
+// the bf16 rounding that follows); for z → −∞ the denominator overflows and the result is 0.
+__device__ __forceinline__ float silu_f32(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 template <typename T>
 __device__ __forceinline__ float to_f32(T v);

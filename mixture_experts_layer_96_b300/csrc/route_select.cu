@@ -1,0 +1,405 @@
+// Routing from fp32 logits: scores, optional group limit, Top-K, gates and the per-block
+// statistics of the aux loss.
+//   [Lesson 10 "专家并行 EP", §1: s(x) = Softmax(TopK(x·W_g, K)) or sigmoid normalisation;
+//    §4: L_aux = α·E·Σ f_i·P_i; §5: a unit's experts restricted to a few groups]
+//
+// Input: the logits as `nparts` fp32 partial sums [part][T'][E] (K slices of the router GEMM, or
+// one array of given logits); they are added in part order, then the logit bias (fp32).
+// Selection keys: softmax → the fp32 logit itself (TopK acts on x·W_g); sigmoid → σ(l) + b
+// formed in fp64. Ties go to the lower expert index (and lower group index). Gates: softmax
+// over the K picked logits, or σ_i/Σσ over the picks (unbiased).
+//
+// Two shapes of kernel:
+//   E <= 64: one thread per unit. A block stages its units' logits in shared memory; each
+//            thread scans its row in expert order keeping a sorted list of its K best
+//            (key, index) (an equal key never displaces a lower index), then overwrites its row
+//            with its probabilities, and the block sums each column in row order.
+//   E > 64:  one warp per unit, each lane E/32 experts; keys are compared as order-preserving
+//            64-bit integers so shuffles and comparisons stay off the fp64 pipe.
+// Both write per-block Σ_t P_{t,i} and pick counts; the aux kernel (route.cu) reduces them.
+#include <math.h>
+
+#include <type_traits>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+constexpr int kSelThreads = 256;
+constexpr int kSelWarpUnits = 32;  // units per block in the warp-per-unit kernel
+
+struct SelectArgs {
+  const float* logits;      // [nparts][Tu][E]
+  int64_t part_stride;
+  int nparts;
+  const float* logit_bias;  // [E] or null
+  const float* select_bias; // [E] or null (sigmoid only)
+  int32_t* idx;             // [Tu][K]
+  float* gate;              // [Tu][K]
+  float* logits_out;        // [Tu][E] or null
+  float* psum_part;         // [blocks][E]
+  int32_t* cnt_part;        // [blocks][E]
+  int64_t Tu;
+  int E, K, n_groups, topk_groups;
+};
+
+__device__ __forceinline__ float load_logit(const SelectArgs& a, int64_t u, int e) {
+  const int64_t o = u * a.E + e;
+  float v = a.logits[o];
+  for (int q = 1; q < a.nparts; ++q) v += a.logits[q * a.part_stride + o];
+  if (a.logit_bias) v = v + a.logit_bias[e];
+  return v;
+}
+
+__device__ __forceinline__ double sigmoid64(float l) { return 1.0 / (1.0 + exp(-(double)l)); }
+
+// Order-preserving map of a double to uint64 (−0 is folded into +0 first).
+__device__ __forceinline__ uint64_t ord64(double d) {
+  d = d + 0.0;
+  const uint64_t u = (uint64_t)__double_as_longlong(d);
+  return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
+}
+
+// ============================================================================ thread per unit
+// units (= threads) per block of the thread-per-unit kernel: the logit tile stays under 48 KB
+template <int EMAX>
+struct SelThreadCfg {
+  static constexpr int T = EMAX <= 32 ? 256 : 128;
+};
+
+// Key of expert e of this thread's unit (the row `row` of the shared tile).
+template <bool SIGMOID>
+__device__ __forceinline__ typename std::conditional<SIGMOID, double, float>::type
+sel_key(const SelectArgs& a, const float* row, int e) {
+  if constexpr (SIGMOID) return sigmoid64(row[e]) + (a.select_bias ? (double)a.select_bias[e] : 0.0);
+  else return row[e];
+}
+
+template <int EMAX, bool SIGMOID>
+__global__ void __launch_bounds__(SelThreadCfg<EMAX>::T)
+select_thread_kernel(SelectArgs a) {
+  using KeyT = typename std::conditional<SIGMOID, double, float>::type;
+  constexpr int kSelThreads = SelThreadCfg<EMAX>::T;
+  constexpr int LD = EMAX + 1;
+  __shared__ float tile[kSelThreads * LD];
+  __shared__ int cnt_s[EMAX];
+  const int tid = threadIdx.x;
+  const int64_t u0 = (int64_t)blockIdx.x * kSelThreads;
+  const int E = a.E, K = a.K;
+  for (int e = tid; e < EMAX; e += kSelThreads) cnt_s[e] = 0;
+  for (int i = tid; i < kSelThreads * E; i += kSelThreads) {
+    const int r = i / E, e = i % E;
+    const int64_t u = u0 + r;
+    const float v = (u < a.Tu) ? load_logit(a, u, e) : 0.f;
+    tile[r * LD + e] = v;
+    if (a.logits_out && u < a.Tu) a.logits_out[u * E + e] = v;
+  }
+  __syncthreads();
+
+  const int64_t u = u0 + tid;
+  const bool valid = u < a.Tu;
+  float* row = tile + tid * LD;
+
+  // group limit: keep the topk_groups groups with the largest sum of their two best keys
+  uint64_t eligible = ~0ull;
+  if (a.n_groups > 1) {
+    const int gs = E / a.n_groups;
+    uint32_t chosen = 0;
+    for (int q = 0; q < a.topk_groups; ++q) {
+      int bg = -1;
+      double bsc = 0.0;
+      for (int g = 0; g < a.n_groups; ++g) {
+        if ((chosen >> g) & 1u) continue;
+        double t1 = -INFINITY, t2 = -INFINITY;
+        for (int i = 0; i < gs; ++i) {
+          const double k = (double)sel_key<SIGMOID>(a, row, g * gs + i);
+          if (k > t1) { t2 = t1; t1 = k; }
+          else if (k > t2) t2 = k;
+        }
+        const double sc = gs > 1 ? t1 + t2 : t1;
+        if (bg < 0 || sc > bsc) { bg = g; bsc = sc; }
+      }
+      chosen |= 1u << bg;
+    }
+    eligible = 0;
+    for (int e = 0; e < E; ++e)
+      if ((chosen >> (e / gs)) & 1u) eligible |= 1ull << e;
+  }
+
+  // Top-K: scan experts in index order; an expert enters when it beats the current K-th key
+  // (strictly: an equal key never displaces an earlier, lower index); it then moves down the
+  // sorted list by (key desc, index asc).
+  KeyT bk[kMaxTopK];
+  int be[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) { bk[j] = (KeyT)-INFINITY; be[j] = -1; }
+  int filled = 0;
+  KeyT worst = (KeyT)-INFINITY;
+  for (int e = 0; e < E; ++e) {
+    if (!((eligible >> e) & 1ull)) continue;
+    KeyT ck = sel_key<SIGMOID>(a, row, e);
+    if (filled == K && !(ck > worst)) continue;
+    int ce = e;
+#pragma unroll
+    for (int t = 0; t < kMaxTopK; ++t) {
+      if (t < K && (be[t] < 0 || ck > bk[t] || (ck == bk[t] && ce < be[t]))) {
+        const KeyT tk = bk[t];
+        const int te = be[t];
+        bk[t] = ck;
+        be[t] = ce;
+        ck = tk;
+        ce = te;
+      }
+    }
+    if (filled < K) ++filled;
+#pragma unroll
+    for (int t = 0; t < kMaxTopK; ++t)
+      if (t == K - 1) worst = bk[t];
+  }
+
+  // gates and picks
+  if (valid) {
+    float lv[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) lv[j] = (j < K && be[j] >= 0) ? row[be[j]] : 0.f;
+    if (SIGMOID) {
+      double sg[kMaxTopK], z = 0.0;
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) { sg[j] = (j < K) ? sigmoid64(lv[j]) : 0.0; z += sg[j]; }
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j)
+        if (j < K) { a.idx[u * K + j] = be[j]; a.gate[u * K + j] = (float)(sg[j] / z); }
+    } else {
+      float ev[kMaxTopK], z = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) { ev[j] = (j < K) ? expf(lv[j] - lv[0]) : 0.f; z += ev[j]; }
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j)
+        if (j < K) { a.idx[u * K + j] = be[j]; a.gate[u * K + j] = ev[j] / z; }
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < K && be[j] >= 0) atomicAdd(&cnt_s[be[j]], 1);
+  }
+
+  // this unit's probabilities replace its logits in the tile; columns are then summed in row order
+  {
+    float m = -INFINITY, z = 0.f;
+    if (!SIGMOID)
+      for (int e = 0; e < E; ++e) m = fmaxf(m, row[e]);
+    for (int e = 0; e < E; ++e) {
+      const float v = SIGMOID ? (float)sigmoid64(row[e]) : expf(row[e] - m);
+      z += v;
+      row[e] = v;
+    }
+    const float iz = valid ? 1.f / z : 0.f;
+    for (int e = 0; e < E; ++e) row[e] *= iz;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kSelThreads) {
+    float s = 0.f;
+    for (int r = 0; r < kSelThreads; ++r) s += tile[r * LD + e];
+    a.psum_part[(int64_t)blockIdx.x * E + e] = s;
+    a.cnt_part[(int64_t)blockIdx.x * E + e] = cnt_s[e];
+  }
+}
+
+// ============================================================================ warp per unit
+template <int EPL, bool SIGMOID>
+__global__ void __launch_bounds__(kSelThreads)
+select_warp_kernel(SelectArgs a) {
+  constexpr int EP = 32 * EPL;
+  __shared__ float psum_w[kSelThreads / 32][EP];
+  __shared__ int cnt_s[EP];
+  __shared__ uint64_t kord_w[kSelThreads / 32][EP];   // ordered keys (group scores)
+  __shared__ double kdbl_w[kSelThreads / 32][EP];     // keys (group sums)
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = a.E, K = a.K;
+  for (int i = tid; i < (kSelThreads / 32) * EP; i += kSelThreads) (&psum_w[0][0])[i] = 0.f;
+  for (int e = tid; e < EP; e += kSelThreads) cnt_s[e] = 0;
+  __syncthreads();
+  const int gs = E / a.n_groups;
+  for (int r = warp; r < kSelWarpUnits; r += kSelThreads / 32) {
+    const int64_t u = (int64_t)blockIdx.x * kSelWarpUnits + r;
+    if (u >= a.Tu) break;
+    float lv[EPL];
+    uint64_t ko[EPL];
+    double kd[EPL];
+    bool valid[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      const int e = lane * EPL + j;
+      valid[j] = e < E;
+      lv[j] = valid[j] ? load_logit(a, u, e) : -INFINITY;
+      if (valid[j] && a.logits_out) a.logits_out[u * E + e] = lv[j];
+      kd[j] = SIGMOID ? (valid[j] ? sigmoid64(lv[j]) + (a.select_bias ? (double)a.select_bias[e] : 0.0) : -INFINITY)
+                      : (double)lv[j];
+      ko[j] = ord64(kd[j]);
+    }
+    // P_i for the aux loss
+    {
+      float pv[EPL], z = 0.f, m = -INFINITY;
+      if (!SIGMOID) {
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) m = fmaxf(m, lv[j]);
+#pragma unroll
+        for (int d = 16; d; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+      }
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
+        pv[j] = !valid[j] ? 0.f : (SIGMOID ? (float)(kd[j] - (a.select_bias ? (double)a.select_bias[lane * EPL + j] : 0.0))
+                                           : expf(lv[j] - m));
+        z += pv[j];
+      }
+#pragma unroll
+      for (int d = 16; d; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
+#pragma unroll
+      for (int j = 0; j < EPL; ++j)
+        if (valid[j]) psum_w[warp][lane * EPL + j] += pv[j] / z;
+    }
+    // group limit
+    uint32_t chosen = 0xffffffffu;
+    if (a.n_groups > 1) {
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
+        kord_w[warp][lane * EPL + j] = ko[j];
+        kdbl_w[warp][lane * EPL + j] = kd[j];
+      }
+      __syncwarp();
+      uint64_t gord = 0;
+      bool gval = false;
+      if (lane < a.n_groups) {
+        int i1 = -1, i2 = -1;
+        uint64_t t1 = 0, t2 = 0;
+        for (int i = 0; i < gs; ++i) {
+          const uint64_t v = kord_w[warp][lane * gs + i];
+          if (i1 < 0 || v > t1) { t2 = t1; i2 = i1; t1 = v; i1 = i; }
+          else if (i2 < 0 || v > t2) { t2 = v; i2 = i; }
+        }
+        const double sc = kdbl_w[warp][lane * gs + i1] + (i2 >= 0 ? kdbl_w[warp][lane * gs + i2] : 0.0);
+        gord = ord64(sc);
+        gval = true;
+      }
+      __syncwarp();
+      chosen = 0;
+      for (int q = 0; q < a.topk_groups; ++q) {
+        const bool cand = gval && !((chosen >> lane) & 1u);
+        uint64_t bk = cand ? gord : 0;
+        int bg = cand ? lane : 0x7fffffff;
+#pragma unroll
+        for (int d = 16; d; d >>= 1) {
+          const uint64_t ok = __shfl_xor_sync(0xffffffffu, bk, d);
+          const int og = __shfl_xor_sync(0xffffffffu, bg, d);
+          if (og != 0x7fffffff && (bg == 0x7fffffff || ok > bk || (ok == bk && og < bg))) { bk = ok; bg = og; }
+        }
+        if (bg != 0x7fffffff) chosen |= 1u << bg;
+      }
+    }
+    // Top-K: K rounds of a warp argmax on (ordered key desc, index asc)
+    bool taken[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) taken[j] = false;
+    int sel_e = -1;
+    for (int q = 0; q < K; ++q) {
+      uint64_t bk = 0;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
+        const int e = lane * EPL + j;
+        const bool elig = valid[j] && !taken[j] && ((chosen >> (e / gs)) & 1u);
+        if (elig && (be == 0x7fffffff || ko[j] > bk)) { bk = ko[j]; be = e; }
+      }
+#pragma unroll
+      for (int d = 16; d; d >>= 1) {
+        const uint64_t ok = __shfl_xor_sync(0xffffffffu, bk, d);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, d);
+        if (oe != 0x7fffffff && (be == 0x7fffffff || ok > bk || (ok == bk && oe < be))) { bk = ok; be = oe; }
+      }
+#pragma unroll
+      for (int j = 0; j < EPL; ++j)
+        if (be == lane * EPL + j) taken[j] = true;
+      if (lane == q) sel_e = (be == 0x7fffffff) ? -1 : be;
+      if (lane == 0 && be != 0x7fffffff) atomicAdd(&cnt_s[be], 1);
+    }
+    // gates from the picked logits
+    float l_sel = (lane < K && sel_e >= 0) ? load_logit(a, u, sel_e) : 0.f;
+    const float l_top = __shfl_sync(0xffffffffu, l_sel, 0);
+    float g;
+    if (SIGMOID) {
+      const double s = (lane < K) ? sigmoid64(l_sel) : 0.0;
+      double z = s;
+#pragma unroll
+      for (int d = 16; d; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
+      g = (float)(s / z);
+    } else {
+      const float ev = (lane < K) ? expf(l_sel - l_top) : 0.f;
+      float z = ev;
+#pragma unroll
+      for (int d = 16; d; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
+      g = ev / z;
+    }
+    if (lane < K) {
+      a.idx[u * K + lane] = sel_e;
+      a.gate[u * K + lane] = g;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kSelThreads) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSelThreads / 32; ++w) s += psum_w[w][e];
+    a.psum_part[(int64_t)blockIdx.x * E + e] = s;
+    a.cnt_part[(int64_t)blockIdx.x * E + e] = cnt_s[e];
+  }
+}
+
+int select_block_units(int E) {
+  return E <= 32 ? SelThreadCfg<32>::T : (E <= 64 ? SelThreadCfg<64>::T : kSelWarpUnits);
+}
+
+template <int EMAX>
+static void launch_thread_sel(const SelectArgs& a, int64_t blocks, bool sigmoid, cudaStream_t s) {
+  constexpr int T = SelThreadCfg<EMAX>::T;
+  if (sigmoid) select_thread_kernel<EMAX, true><<<(unsigned)blocks, T, 0, s>>>(a);
+  else select_thread_kernel<EMAX, false><<<(unsigned)blocks, T, 0, s>>>(a);
+}
+
+template <int EPL>
+static void launch_warp_sel(const SelectArgs& a, int64_t blocks, bool sigmoid, cudaStream_t s) {
+  if (sigmoid) select_warp_kernel<EPL, true><<<(unsigned)blocks, kSelThreads, 0, s>>>(a);
+  else select_warp_kernel<EPL, false><<<(unsigned)blocks, kSelThreads, 0, s>>>(a);
+}
+
+cudaError_t launch_select(const Problem& p, const float* logits, int nparts, int64_t part_stride,
+                          const float* logit_bias, const float* select_bias, int32_t* idx, float* gate,
+                          float* logits_out, float* psum_part, int32_t* cnt_part, cudaStream_t s) {
+  if (p.Tu == 0) return cudaSuccess;
+  SelectArgs a;
+  a.logits = logits;
+  a.part_stride = part_stride;
+  a.nparts = nparts;
+  a.logit_bias = logit_bias;
+  a.select_bias = p.sigmoid ? select_bias : nullptr;
+  a.idx = idx;
+  a.gate = gate;
+  a.logits_out = logits_out;
+  a.psum_part = psum_part;
+  a.cnt_part = cnt_part;
+  a.Tu = p.Tu;
+  a.E = p.E;
+  a.K = p.K;
+  a.n_groups = p.n_groups;
+  a.topk_groups = p.topk_groups;
+  const int64_t blocks = p.route_blocks;
+  if (p.E <= 8) launch_thread_sel<8>(a, blocks, p.sigmoid, s);
+  else if (p.E <= 16) launch_thread_sel<16>(a, blocks, p.sigmoid, s);
+  else if (p.E <= 32) launch_thread_sel<32>(a, blocks, p.sigmoid, s);
+  else if (p.E <= 64) launch_thread_sel<64>(a, blocks, p.sigmoid, s);
+  else if (p.E <= 128) launch_warp_sel<4>(a, blocks, p.sigmoid, s);
+  else launch_warp_sel<8>(a, blocks, p.sigmoid, s);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe
