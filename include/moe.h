@@ -194,8 +194,10 @@ MOE_API int32_t moe_abi_version(void);
  *    that device current) and keeps it; make that first call before any stream capture.
  *  - It allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  *  - All calls on a device share the array, which keeps the last call's contents; each call
- *    rewrites every part it reads, so nothing needs clearing, but calls that overlap on the GPU
- *    (e.g. on two streams) race and give wrong results. Serialise them.
+ *    rewrites every part it reads before reading it, and the one counter in it (zero when the
+ *    library loads) is back at zero when a call's kernels finish, so nothing needs clearing.
+ *    Calls that overlap on the GPU (e.g. on two streams) race and give wrong results: serialise
+ *    them.
  *  - Bad indices (out of range or repeated within a unit) give that unit slot -1 for every pick,
  *    as in moe_dispatch, but are not reported: there is no workspace status word here. */
 MOE_API moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const void* x,

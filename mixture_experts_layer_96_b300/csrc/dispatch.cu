@@ -6,8 +6,8 @@
 // pick (t,k) in expert e's queue is the number of earlier units that picked e: a stable counting
 // sort. Four kernels, no atomics whose order matters and no inter-block waits:
 //   1. hist:   per chunk of 256 units, picks per expert (and index validation)
-//   2. scan:   one block: per-expert totals (pre-drop counts), each chunk's base in each queue,
-//              kept rows n_e = min(count, C) and their exclusive scan (offsets)
+//   2. scan:   a block per expert: per-expert totals (pre-drop counts) and each chunk's base in
+//              each queue; the last block scans the kept rows n_e = min(count, C) into offsets
 //   3. rank:   per chunk, each pick's place = chunk base + earlier warps' picks + earlier lanes'
 //              picks (a per-warp bitmask of the lanes that picked each expert); writes slot_of,
 //              row_token and -1 into row_token past the kept rows
@@ -45,52 +45,85 @@ dispatch_hist_kernel(const int32_t* __restrict__ idx, int64_t Tu, int K, int E,
   for (int e = tid; e < E; e += kChunk) chunk_hist[(int64_t)blockIdx.x * E + e] = cnt[e];
 }
 
-// One block of 256 threads; thread e walks the chunks of expert e in order.
-__global__ void __launch_bounds__(256)
+// One block per expert: an exclusive scan of the expert's column of chunk counts (one chunk per
+// thread per pass, a block scan per pass) gives each chunk's base in the expert's queue and the
+// pre-drop count. The last block to finish (ticket) scans the kept rows n_e = min(count_e, C)
+// over experts into the offsets and resets the ticket. Integer sums, so the result does not
+// depend on which block finishes last.
+constexpr int kScanThreads = 256;
+
+__global__ void __launch_bounds__(kScanThreads)
 dispatch_scan_kernel(const int32_t* __restrict__ chunk_hist, int64_t nchunks, int E, int64_t C,
                      int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts_ws,
-                     int32_t* __restrict__ offsets_ws, int32_t* counts_out, int32_t* offsets_out) {
-  __shared__ int kept[kMaxExperts];
+                     int32_t* __restrict__ offsets_ws, int32_t* counts_out, int32_t* offsets_out,
+                     unsigned int* ticket) {
+  __shared__ int warp_tot[kScanThreads / 32];
   __shared__ int excl[kMaxExperts + 1];
-  const int e = threadIdx.x;
-  if (e < E) {
-    int run = 0;
-    for (int64_t c = 0; c < nchunks; ++c) {
-      chunk_base[c * E + e] = run;
-      run += chunk_hist[c * E + e];
-    }
-    counts_ws[e] = run;
-    if (counts_out) counts_out[e] = run;
-    kept[e] = (int)((int64_t)run < C ? (int64_t)run : C);
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {  // warp scan of kept over E <= 256 (8 per lane)
-    const int lane = threadIdx.x;
-    int loc[8], s = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int ee = lane * 8 + j;
-      loc[j] = s;
-      s += (ee < E) ? kept[ee] : 0;
-    }
-    int incl = s;
+  __shared__ bool last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int e = blockIdx.x;
+  int carry = 0;
+  for (int64_t c0 = 0; c0 < nchunks; c0 += kScanThreads) {
+    const int64_t c = c0 + tid;
+    const int v = c < nchunks ? chunk_hist[c * E + e] : 0;
+    int incl = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += v;
+      const int t = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += t;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int before = 0, pass_total = 0;
+#pragma unroll
+    for (int w = 0; w < kScanThreads / 32; ++w) {
+      before += (w < warp) ? warp_tot[w] : 0;
+      pass_total += warp_tot[w];
+    }
+    if (c < nchunks) chunk_base[c * E + e] = carry + before + incl - v;
+    carry += pass_total;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    counts_ws[e] = carry;
+    if (counts_out) counts_out[e] = carry;
+    __threadfence();
+    last = atomicAdd(ticket, 1u) == (unsigned)(E - 1);
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (tid < 32) {  // warp scan of kept over E <= 256 (8 per lane)
+    const volatile int32_t* cnt = counts_ws;
+    int loc[8], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int ee = lane * 8 + j;
+      loc[j] = sum;
+      if (ee < E) {
+        const int64_t n = cnt[ee];
+        sum += (int)(n < C ? n : C);
+      }
+    }
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += t;
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int ee = lane * 8 + j;
-      if (ee < E) excl[ee] = incl - s + loc[j];
+      if (ee < E) excl[ee] = incl - sum + loc[j];
     }
     if (lane == 31) excl[E] = incl;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+  for (int i = tid; i <= E; i += kScanThreads) {
     offsets_ws[i] = excl[i];
     if (offsets_out) offsets_out[i] = excl[i];
   }
+  if (tid == 0) *ticket = 0u;
 }
 
 __global__ void __launch_bounds__(kChunk)
@@ -146,28 +179,34 @@ dispatch_rank_kernel(const int32_t* __restrict__ idx, int64_t Tu, int K, int E, 
     row_token[r] = -1;
 }
 
-// x_packed[r] = x[row_token[r]] for r < offsets[E]; rows are `row_bytes` long (multiple of 16).
+// x_packed[r] = x[row_token[r]] for r < offsets[E]; rows are `row_vecs` 16-byte vectors. The
+// packed rows are one flat array of vectors; each warp copies 128 consecutive vectors per step
+// (vector wb + 32·j + lane, j = 0..3), so every load and store instruction covers 512 contiguous
+// bytes, with four independent loads in flight per lane whatever the row length.
 __global__ void __launch_bounds__(256)
 dispatch_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row_token,
                        const int32_t* __restrict__ offsets, int E, int64_t row_vecs,
                        uint4* __restrict__ x_packed) {
-  const int64_t kept = offsets[E];
-  const int lane = threadIdx.x & 31;
-  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < kept; r += warps) {
-    const int64_t t = row_token[r];
-    const uint4* src = x + t * row_vecs;
-    uint4* dst = x_packed + r * row_vecs;
-    int64_t v = lane;
-    for (; v + 96 < row_vecs; v += 128) {  // four 16-byte loads in flight per lane
-      const uint4 a0 = __ldg(src + v), a1 = __ldg(src + v + 32), a2 = __ldg(src + v + 64),
-                  a3 = __ldg(src + v + 96);
-      dst[v] = a0;
-      dst[v + 32] = a1;
-      dst[v + 64] = a2;
-      dst[v + 96] = a3;
+  const uint32_t rv = (uint32_t)row_vecs;
+  const uint64_t total = (uint64_t)offsets[E] * rv;
+  const uint64_t nwarps = (uint64_t)gridDim.x * (blockDim.x >> 5);
+  const uint32_t lane = threadIdx.x & 31u;
+  for (uint64_t wb = ((uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 128u; wb < total;
+       wb += nwarps * 128u) {
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint64_t i = wb + 32u * j + lane;
+      if (i < total) {
+        const uint64_t r = i / rv;
+        v[j] = __ldg(x + (int64_t)__ldg(row_token + r) * row_vecs + (i - r * rv));
+      }
     }
-    for (; v < row_vecs; v += 32) dst[v] = __ldg(src + v);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint64_t i = wb + 32u * j + lane;
+      if (i < total) x_packed[i] = v[j];
+    }
   }
 }
 
@@ -198,8 +237,9 @@ cudaError_t launch_dispatch(const Problem& p, const void* x, const int32_t* idx,
     dispatch_hist_kernel<<<nch, kChunk, 0, s>>>(idx, p.Tu, p.K, p.E, chunk_hist, status);
     note_launch();
   }
-  dispatch_scan_kernel<<<1, 256, 0, s>>>(chunk_hist, p.nchunks, p.E, p.C, chunk_base, counts_ws,
-                                         offsets_ws, counts, offsets);
+  dispatch_scan_kernel<<<p.E, kScanThreads, 0, s>>>(chunk_hist, p.nchunks, p.E, p.C, chunk_base,
+                                                    counts_ws, offsets_ws, counts, offsets,
+                                                    ws_ptr<unsigned int>(ws, L.status + 8));
   note_launch();
   const int64_t rows = p.rows;
   const unsigned rank_blocks = nch > 0 ? nch : 1;
@@ -209,8 +249,7 @@ cudaError_t launch_dispatch(const Problem& p, const void* x, const int32_t* idx,
   if (rows > 0) {
     const int64_t row_bytes = (int64_t)p.hu * (int64_t)p.elt;
     const int sms = device_sm_count();
-    const int64_t warps_needed = rows;
-    int64_t blocks = (warps_needed + 7) / 8;
+    int64_t blocks = (rows * (row_bytes / 16) + 1023) / 1024;
     const int64_t cap = (int64_t)sms * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;

@@ -6,8 +6,9 @@
 // copy until the process exits. Host code cannot use the array's name as a device address, so the
 // first call on each device looks the address up with cudaGetSymbolAddress (with that device
 // current) and caches it; kernels get that pointer. Every region of the array is fully written by
-// one kernel of a call before a later kernel of the same call reads it, so no clearing is needed;
-// two calls that overlap on the GPU share the array and race.
+// one kernel of a call before a later kernel of the same call reads it, and the scan's ticket
+// counter returns to zero at the end of each call, so no clearing is needed; two calls that
+// overlap on the GPU share the array and race.
 #include <mutex>
 
 #include "moe_device.cuh"
@@ -21,7 +22,7 @@ __global__ void dispatch_hist_kernel(const int32_t* __restrict__ idx, int64_t Tu
 __global__ void dispatch_scan_kernel(const int32_t* __restrict__ chunk_hist, int64_t nchunks, int E,
                                      int64_t C, int32_t* __restrict__ chunk_base,
                                      int32_t* __restrict__ counts_ws, int32_t* __restrict__ offsets_ws,
-                                     int32_t* counts_out, int32_t* offsets_out);
+                                     int32_t* counts_out, int32_t* offsets_out, unsigned int* ticket);
 __global__ void dispatch_rank_kernel(const int32_t* __restrict__ idx, int64_t Tu, int K, int E, int64_t C,
                                      const int32_t* __restrict__ chunk_base,
                                      const int32_t* __restrict__ offsets, int32_t* __restrict__ slot_of,
@@ -77,13 +78,17 @@ extern "C" MOE_API moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, co
   if (p.Tu > 0 && (!x || !topk_idx || !slot_of || !row_token || !x_packed)) return MOE_ERR_INVALID_ARG;
   const size_t E = (size_t)p.E;
   const size_t hist_bytes = align256((size_t)p.nchunks * E * 4);
-  const size_t off_counts = 0, off_offsets = align256(E * 4), off_hist = off_offsets + align256((E + 1) * 4);
+  // [ticket (256 B) | counts | offsets | chunk histograms | chunk bases]; the ticket is zero at
+  // load time and the scan's last block resets it, so it is zero at the start of every call
+  const size_t off_ticket = 0, off_counts = 256, off_offsets = off_counts + align256(E * 4);
+  const size_t off_hist = off_offsets + align256((E + 1) * 4);
   const size_t off_base = off_hist + hist_bytes;
   if (off_base + hist_bytes > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
 
   void* base = nullptr;
   if (scratch_address(&base) != cudaSuccess) return MOE_ERR_CUDA;
   char* sc = static_cast<char*>(base);
+  unsigned int* ticket = reinterpret_cast<unsigned int*>(sc + off_ticket);
   int32_t* counts_ws = reinterpret_cast<int32_t*>(sc + off_counts);
   int32_t* offsets_ws = reinterpret_cast<int32_t*>(sc + off_offsets);
   int32_t* chunk_hist = reinterpret_cast<int32_t*>(sc + off_hist);
@@ -95,16 +100,17 @@ extern "C" MOE_API moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, co
     dispatch_hist_kernel<<<nch, kChunk, 0, s>>>(topk_idx, p.Tu, p.K, p.E, chunk_hist, nullptr);
     note_launch();
   }
-  dispatch_scan_kernel<<<1, 256, 0, s>>>(chunk_hist, p.nchunks, p.E, p.C, chunk_base, counts_ws,
-                                         offsets_ws, counts, offsets);
+  dispatch_scan_kernel<<<p.E, 256, 0, s>>>(chunk_hist, p.nchunks, p.E, p.C, chunk_base, counts_ws,
+                                          offsets_ws, counts, offsets, ticket);
   note_launch();
   dispatch_rank_kernel<<<nch > 0 ? nch : 1, kChunk, 0, s>>>(topk_idx, p.Tu, p.K, p.E, p.C, chunk_base,
                                                            offsets_ws, slot_of, row_token, p.rows);
   note_launch();
   if (p.rows > 0) {
     const int64_t row_bytes = (int64_t)p.hu * (int64_t)p.elt;
-    int64_t blocks = (p.rows + 7) / 8;
+    int64_t blocks = (p.rows * (row_bytes / 16) + 1023) / 1024;
     const int64_t cap = (int64_t)device_sm_count() * 8;
+    if (blocks < 1) blocks = 1;
     if (blocks > cap) blocks = cap;
     if (row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
         (reinterpret_cast<uintptr_t>(x_packed) & 15) == 0) {

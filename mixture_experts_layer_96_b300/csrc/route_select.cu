@@ -61,6 +61,59 @@ __device__ __forceinline__ uint64_t ord64(double d) {
   return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
 }
 
+// Stage the logits of units [u0, u0+rows) into tile[r*LD + e] (partials added in order, then the
+// logit bias), and copy them to logits_out if asked. Rows are loaded as float4 with several loads
+// in flight per thread when E is a multiple of 4; otherwise one float at a time.
+template <int NT, int LD>
+__device__ __forceinline__ void stage_logits(const SelectArgs& a, int64_t u0, float* tile) {
+  const int E = a.E, tid = threadIdx.x;
+  const int64_t rows = (a.Tu - u0) < NT ? (a.Tu - u0) : NT;
+  if ((E & 3) == 0) {
+    const int per_row = E >> 2;
+    const int n4 = (int)rows * per_row;
+    constexpr int U = 8;
+    for (int base = tid; base < n4; base += NT * U) {
+      float4 v[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const int i = base + j * NT;
+        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < n4) v[j] = __ldg(reinterpret_cast<const float4*>(a.logits + u0 * E) + i);
+      }
+      for (int q = 1; q < a.nparts; ++q) {
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          const int i = base + j * NT;
+          if (i < n4) {
+            const float4 w = __ldg(reinterpret_cast<const float4*>(a.logits + q * a.part_stride + u0 * E) + i);
+            v[j].x += w.x; v[j].y += w.y; v[j].z += w.z; v[j].w += w.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const int i = base + j * NT;
+        if (i >= n4) break;
+        const int r = i / per_row, e = (i - r * per_row) * 4;
+        float4 w = v[j];
+        if (a.logit_bias) {
+          w.x = w.x + a.logit_bias[e]; w.y = w.y + a.logit_bias[e + 1];
+          w.z = w.z + a.logit_bias[e + 2]; w.w = w.w + a.logit_bias[e + 3];
+        }
+        tile[r * LD + e] = w.x; tile[r * LD + e + 1] = w.y; tile[r * LD + e + 2] = w.z; tile[r * LD + e + 3] = w.w;
+        if (a.logits_out) reinterpret_cast<float4*>(a.logits_out + u0 * E)[i] = w;
+      }
+    }
+  } else {
+    for (int i = tid; i < rows * E; i += NT) {
+      const int r = i / E, e = i % E;
+      const float v = load_logit(a, u0 + r, e);
+      tile[r * LD + e] = v;
+      if (a.logits_out) a.logits_out[(u0 + r) * E + e] = v;
+    }
+  }
+}
+
 // ============================================================================ thread per unit
 // units (= threads) per block of the thread-per-unit kernel: the logit tile stays under 48 KB
 template <int EMAX>
@@ -76,7 +129,7 @@ sel_key(const SelectArgs& a, const float* row, int e) {
   else return row[e];
 }
 
-template <int EMAX, bool SIGMOID>
+template <int EMAX, int KMAX, bool SIGMOID>
 __global__ void __launch_bounds__(SelThreadCfg<EMAX>::T)
 select_thread_kernel(SelectArgs a) {
   using KeyT = typename std::conditional<SIGMOID, double, float>::type;
@@ -88,13 +141,7 @@ select_thread_kernel(SelectArgs a) {
   const int64_t u0 = (int64_t)blockIdx.x * kSelThreads;
   const int E = a.E, K = a.K;
   for (int e = tid; e < EMAX; e += kSelThreads) cnt_s[e] = 0;
-  for (int i = tid; i < kSelThreads * E; i += kSelThreads) {
-    const int r = i / E, e = i % E;
-    const int64_t u = u0 + r;
-    const float v = (u < a.Tu) ? load_logit(a, u, e) : 0.f;
-    tile[r * LD + e] = v;
-    if (a.logits_out && u < a.Tu) a.logits_out[u * E + e] = v;
-  }
+  stage_logits<kSelThreads, LD>(a, u0, tile);
   __syncthreads();
 
   const int64_t u = u0 + tid;
@@ -127,59 +174,50 @@ select_thread_kernel(SelectArgs a) {
       if ((chosen >> (e / gs)) & 1u) eligible |= 1ull << e;
   }
 
-  // Top-K: scan experts in index order; an expert enters when it beats the current K-th key
-  // (strictly: an equal key never displaces an earlier, lower index); it then moves down the
-  // sorted list by (key desc, index asc).
-  KeyT bk[kMaxTopK];
-  int be[kMaxTopK];
+  // Top-K: scan experts in index order keeping bk[0..K) sorted by key, descending. A new key is
+  // placed below every kept key that is >= it (an equal key never displaces an earlier, lower
+  // index), the entries it passes shift down one slot. Slots are filled in order; be = -1 marks
+  // an empty slot.
+  KeyT bk[KMAX];
+  int be[KMAX];
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) { bk[j] = (KeyT)-INFINITY; be[j] = -1; }
-  int filled = 0;
-  KeyT worst = (KeyT)-INFINITY;
+  for (int j = 0; j < KMAX; ++j) { bk[j] = (KeyT)-INFINITY; be[j] = -1; }
   for (int e = 0; e < E; ++e) {
     if (!((eligible >> e) & 1ull)) continue;
-    KeyT ck = sel_key<SIGMOID>(a, row, e);
-    if (filled == K && !(ck > worst)) continue;
-    int ce = e;
+    const KeyT ck = sel_key<SIGMOID>(a, row, e);
 #pragma unroll
-    for (int t = 0; t < kMaxTopK; ++t) {
-      if (t < K && (be[t] < 0 || ck > bk[t] || (ck == bk[t] && ce < be[t]))) {
-        const KeyT tk = bk[t];
-        const int te = be[t];
-        bk[t] = ck;
-        be[t] = ce;
-        ck = tk;
-        ce = te;
+    for (int t = KMAX - 1; t >= 0; --t) {
+      if (t < K) {
+        const bool above = t > 0 && (be[t - 1] < 0 || ck > bk[t - 1]);
+        const bool here = be[t] < 0 || ck > bk[t];
+        if (above) { bk[t] = bk[t - 1]; be[t] = be[t - 1]; }
+        else if (here) { bk[t] = ck; be[t] = e; }
       }
     }
-    if (filled < K) ++filled;
-#pragma unroll
-    for (int t = 0; t < kMaxTopK; ++t)
-      if (t == K - 1) worst = bk[t];
   }
 
   // gates and picks
   if (valid) {
-    float lv[kMaxTopK];
+    float lv[KMAX];
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) lv[j] = (j < K && be[j] >= 0) ? row[be[j]] : 0.f;
+    for (int j = 0; j < KMAX; ++j) lv[j] = (j < K && be[j] >= 0) ? row[be[j]] : 0.f;
     if (SIGMOID) {
-      double sg[kMaxTopK], z = 0.0;
+      double sg[KMAX], z = 0.0;
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) { sg[j] = (j < K) ? sigmoid64(lv[j]) : 0.0; z += sg[j]; }
+      for (int j = 0; j < KMAX; ++j) { sg[j] = (j < K) ? sigmoid64(lv[j]) : 0.0; z += sg[j]; }
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j)
+      for (int j = 0; j < KMAX; ++j)
         if (j < K) { a.idx[u * K + j] = be[j]; a.gate[u * K + j] = (float)(sg[j] / z); }
     } else {
-      float ev[kMaxTopK], z = 0.f;
+      float ev[KMAX], z = 0.f;
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) { ev[j] = (j < K) ? expf(lv[j] - lv[0]) : 0.f; z += ev[j]; }
+      for (int j = 0; j < KMAX; ++j) { ev[j] = (j < K) ? expf(lv[j] - lv[0]) : 0.f; z += ev[j]; }
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j)
+      for (int j = 0; j < KMAX; ++j)
         if (j < K) { a.idx[u * K + j] = be[j]; a.gate[u * K + j] = ev[j] / z; }
     }
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j)
+    for (int j = 0; j < KMAX; ++j)
       if (j < K && be[j] >= 0) atomicAdd(&cnt_s[be[j]], 1);
   }
 
@@ -189,19 +227,34 @@ select_thread_kernel(SelectArgs a) {
     if (!SIGMOID)
       for (int e = 0; e < E; ++e) m = fmaxf(m, row[e]);
     for (int e = 0; e < E; ++e) {
-      const float v = SIGMOID ? (float)sigmoid64(row[e]) : expf(row[e] - m);
+      const float v = SIGMOID ? (float)sigmoid64(row[e]) : __expf(row[e] - m);
       z += v;
       row[e] = v;
     }
     const float iz = valid ? 1.f / z : 0.f;
-    for (int e = 0; e < E; ++e) row[e] *= iz;
+    for (int e = 0; e < E; ++e) row[e] = valid ? row[e] * iz : 0.f;
   }
   __syncthreads();
-  for (int e = tid; e < E; e += kSelThreads) {
+  // column sums: P threads per column, each over a contiguous block of rows, then the P partial
+  // sums of a column in order (fixed order, so deterministic)
+  __shared__ float colpart[kSelThreads];
+  {
+    const int P = kSelThreads / E;  // >= 2 for E <= 64
+    const int e = tid / P, part = tid % P;
+    const int rows_per = (kSelThreads + P - 1) / P;
     float s = 0.f;
-    for (int r = 0; r < kSelThreads; ++r) s += tile[r * LD + e];
-    a.psum_part[(int64_t)blockIdx.x * E + e] = s;
-    a.cnt_part[(int64_t)blockIdx.x * E + e] = cnt_s[e];
+    if (e < E) {
+      const int r0 = part * rows_per, r1 = min(kSelThreads, r0 + rows_per);
+      for (int r = r0; r < r1; ++r) s += tile[r * LD + e];
+    }
+    colpart[tid] = s;
+    __syncthreads();
+    if (tid < E) {
+      float t = 0.f;
+      for (int q = 0; q < P; ++q) t += colpart[tid * P + q];
+      a.psum_part[(int64_t)blockIdx.x * E + tid] = t;
+      a.cnt_part[(int64_t)blockIdx.x * E + tid] = cnt_s[tid];
+    }
   }
 }
 
@@ -358,11 +411,18 @@ int select_block_units(int E) {
   return E <= 32 ? SelThreadCfg<32>::T : (E <= 64 ? SelThreadCfg<64>::T : kSelWarpUnits);
 }
 
+template <int EMAX, int KMAX>
+static void launch_thread_sel_k(const SelectArgs& a, int64_t blocks, bool sigmoid, cudaStream_t s) {
+  constexpr int T = SelThreadCfg<EMAX>::T;
+  if (sigmoid) select_thread_kernel<EMAX, KMAX, true><<<(unsigned)blocks, T, 0, s>>>(a);
+  else select_thread_kernel<EMAX, KMAX, false><<<(unsigned)blocks, T, 0, s>>>(a);
+}
+
 template <int EMAX>
 static void launch_thread_sel(const SelectArgs& a, int64_t blocks, bool sigmoid, cudaStream_t s) {
-  constexpr int T = SelThreadCfg<EMAX>::T;
-  if (sigmoid) select_thread_kernel<EMAX, true><<<(unsigned)blocks, T, 0, s>>>(a);
-  else select_thread_kernel<EMAX, false><<<(unsigned)blocks, T, 0, s>>>(a);
+  if (a.K <= 2) launch_thread_sel_k<EMAX, 2>(a, blocks, sigmoid, s);
+  else if (a.K <= 4) launch_thread_sel_k<EMAX, 4>(a, blocks, sigmoid, s);
+  else launch_thread_sel_k<EMAX, 8>(a, blocks, sigmoid, s);
 }
 
 template <int EPL>
