@@ -203,13 +203,17 @@ aux_finalize_kernel(const float* __restrict__ psum_part, const int32_t* __restri
     last = atomicAdd(ticket, 1u) == (unsigned)(E - 1);
   }
   __syncthreads();
-  if (last && tid == 0) {
+  if (last) {
     __threadfence();
     const volatile double* vt = terms;
-    double acc = 0.0;
-    for (int i = 0; i < E; ++i) acc += vt[i];
-    *aux_out = (float)((double)alpha * E * acc);
-    *ticket = 0u;
+    for (int i = tid; i < E; i += 256) sP[i] = vt[i];  // all E terms, loaded in parallel
+    __syncthreads();
+    if (tid == 0) {
+      double acc = 0.0;
+      for (int i = 0; i < E; ++i) acc += sP[i];  // expert order
+      *aux_out = (float)((double)alpha * E * acc);
+      *ticket = 0u;
+    }
   }
 }
 

@@ -27,7 +27,7 @@
 namespace moe {
 
 constexpr int kSelThreads = 256;
-constexpr int kSelWarpUnits = 32;  // units per block in the warp-per-unit kernel
+constexpr int kSelWarpUnits = 8;  // units per block in the warp-per-unit kernel (one per warp)
 
 struct SelectArgs {
   const float* logits;      // [nparts][Tu][E]
@@ -112,6 +112,30 @@ __device__ __forceinline__ void stage_logits(const SelectArgs& a, int64_t u0, fl
       if (a.logits_out) a.logits_out[(u0 + r) * E + e] = v;
     }
   }
+}
+
+// Order-preserving map of a float to uint32 (−0 folded into +0).
+__device__ __forceinline__ uint32_t ord32(float f) {
+  f = f + 0.0f;
+  const uint32_t u = __float_as_uint(f);
+  return (u >> 31) ? ~u : (u | 0x80000000u);
+}
+
+// Warp argmax on (ordered key desc, index asc) over candidates; returns the winner's index or
+// 0x7fffffff (none) and its key.
+__device__ __forceinline__ int warp_argmax32(uint32_t k, int idx, uint32_t& best_k) {
+#pragma unroll
+  for (int d = 16; d; d >>= 1) {
+    const uint32_t ok = __shfl_xor_sync(0xffffffffu, k, d);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, d);
+    if (oi != 0x7fffffff && (idx == 0x7fffffff || ok > k || (ok == k && oi < idx))) { k = ok; idx = oi; }
+  }
+  best_k = k;
+  return idx;
+}
+
+__device__ __forceinline__ float unord32(uint32_t u) {
+  return __uint_as_float((u >> 31) ? (u & 0x7fffffffu) : ~u);
 }
 
 // ============================================================================ thread per unit
@@ -280,15 +304,126 @@ select_warp_kernel(SelectArgs a) {
     uint64_t ko[EPL];
     double kd[EPL];
     bool valid[EPL];
+    if ((E & 3) == 0 && (EPL & 3) == 0 && lane * EPL + EPL <= E) {
+      // a lane's EPL experts are contiguous: float4 loads, every part's loads issued together
+      const float4* src = reinterpret_cast<const float4*>(a.logits + u * E + lane * EPL);
+      float4 v[EPL / 4];
+#pragma unroll
+      for (int j = 0; j < EPL / 4; ++j) v[j] = __ldg(src + j);
+      for (int q = 1; q < a.nparts; ++q) {
+        float4 w[EPL / 4];
+#pragma unroll
+        for (int j = 0; j < EPL / 4; ++j) w[j] = __ldg(src + (q * a.part_stride) / 4 + j);
+#pragma unroll
+        for (int j = 0; j < EPL / 4; ++j) { v[j].x += w[j].x; v[j].y += w[j].y; v[j].z += w[j].z; v[j].w += w[j].w; }
+      }
+#pragma unroll
+      for (int j = 0; j < EPL / 4; ++j) {
+        lv[4 * j] = v[j].x; lv[4 * j + 1] = v[j].y; lv[4 * j + 2] = v[j].z; lv[4 * j + 3] = v[j].w;
+      }
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
+        const int e = lane * EPL + j;
+        valid[j] = true;
+        if (a.logit_bias) lv[j] = lv[j] + a.logit_bias[e];
+        if (a.logits_out) a.logits_out[u * E + e] = lv[j];
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
+        const int e = lane * EPL + j;
+        valid[j] = e < E;
+        lv[j] = valid[j] ? load_logit(a, u, e) : -INFINITY;
+        if (valid[j] && a.logits_out) a.logits_out[u * E + e] = lv[j];
+      }
+    }
+    // Sigmoid keys σ(l)+b are decided in fp64. First screen in fp32: |key32 − key64| <= 4.3e-7
+    // (accurate expf, IEEE divide, one rounding of the add), so when every decision's fp32 margin
+    // exceeds twice the error bound (group scores: two keys and a rounded add each) the fp32
+    // decisions equal the fp64 ones; otherwise this unit takes the fp64 path below.
+    int sel_e = -1;
+    bool screened = false;
+    uint32_t chosen = 0xffffffffu;
+    if (SIGMOID) {
+      constexpr float kDelta = 1e-6f;
+      float k32[EPL];
+      uint32_t o32[EPL];
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
+        const int e = lane * EPL + j;
+        k32[j] = valid[j] ? (1.0f / (1.0f + expf(-lv[j]))) + (a.select_bias ? a.select_bias[e] : 0.0f) : -INFINITY;
+        o32[j] = ord32(k32[j]);
+      }
+      bool safe = true;
+      if (a.n_groups > 1) {
+        float* gk = reinterpret_cast<float*>(&kdbl_w[warp][0]);
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) gk[lane * EPL + j] = k32[j];
+        __syncwarp();
+        uint32_t gord = 0;
+        int gidx = 0x7fffffff;
+        if (lane < a.n_groups) {
+          float t1 = -INFINITY, t2 = -INFINITY;
+          for (int i = 0; i < gs; ++i) {
+            const float v = gk[lane * gs + i];
+            if (v > t1) { t2 = t1; t1 = v; }
+            else if (v > t2) t2 = v;
+          }
+          gord = ord32(gs > 1 ? t1 + t2 : t1);
+          gidx = lane;
+        }
+        __syncwarp();
+        chosen = 0;
+        float last_sc = 0.f;
+        for (int q = 0; q <= a.topk_groups && q < a.n_groups; ++q) {
+          const bool cand = gidx != 0x7fffffff && !((chosen >> lane) & 1u);
+          uint32_t bk;
+          const int bg = warp_argmax32(cand ? gord : 0u, cand ? gidx : 0x7fffffff, bk);
+          const float sc = unord32(bk);
+          if (q < a.topk_groups) {
+            chosen |= 1u << bg;
+            last_sc = sc;
+          } else if (!(last_sc - sc > 4.0f * kDelta + 4.0e-7f)) {
+            safe = false;
+          }
+        }
+      }
+      bool taken[EPL];
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) taken[j] = false;
+      float prev = 0.f;
+      for (int q = 0; q <= a.K; ++q) {
+        uint32_t bk = 0;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+          const int e = lane * EPL + j;
+          const bool elig = valid[j] && !taken[j] && ((chosen >> (e / gs)) & 1u);
+          if (elig && (be == 0x7fffffff || o32[j] > bk)) { bk = o32[j]; be = e; }
+        }
+        uint32_t wk;
+        be = warp_argmax32(bk, be, wk);
+        if (be == 0x7fffffff) break;  // fewer than K+1 eligible experts: no further margin
+        const float kv = unord32(wk);
+        if (q > 0 && !(prev - kv > 2.0f * kDelta)) safe = false;
+        prev = kv;
+        if (q < a.K) {
+#pragma unroll
+          for (int j = 0; j < EPL; ++j)
+            if (be == lane * EPL + j) taken[j] = true;
+          if (lane == q) sel_e = be;
+        }
+      }
+      screened = safe;
+    }
+    if (!screened) {
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
       const int e = lane * EPL + j;
-      valid[j] = e < E;
-      lv[j] = valid[j] ? load_logit(a, u, e) : -INFINITY;
-      if (valid[j] && a.logits_out) a.logits_out[u * E + e] = lv[j];
       kd[j] = SIGMOID ? (valid[j] ? sigmoid64(lv[j]) + (a.select_bias ? (double)a.select_bias[e] : 0.0) : -INFINITY)
                       : (double)lv[j];
       ko[j] = ord64(kd[j]);
+    }
     }
     // P_i for the aux loss
     {
@@ -301,8 +436,7 @@ select_warp_kernel(SelectArgs a) {
       }
 #pragma unroll
       for (int j = 0; j < EPL; ++j) {
-        pv[j] = !valid[j] ? 0.f : (SIGMOID ? (float)(kd[j] - (a.select_bias ? (double)a.select_bias[lane * EPL + j] : 0.0))
-                                           : expf(lv[j] - m));
+        pv[j] = !valid[j] ? 0.f : (SIGMOID ? 1.0f / (1.0f + expf(-lv[j])) : expf(lv[j] - m));
         z += pv[j];
       }
 #pragma unroll
@@ -311,8 +445,10 @@ select_warp_kernel(SelectArgs a) {
       for (int j = 0; j < EPL; ++j)
         if (valid[j]) psum_w[warp][lane * EPL + j] += pv[j] / z;
     }
+    // fp64 decision (all softmax units; sigmoid units whose fp32 screen was not conclusive)
+    if (!screened) {
     // group limit
-    uint32_t chosen = 0xffffffffu;
+    chosen = 0xffffffffu;
     if (a.n_groups > 1) {
 #pragma unroll
       for (int j = 0; j < EPL; ++j) {
@@ -353,7 +489,6 @@ select_warp_kernel(SelectArgs a) {
     bool taken[EPL];
 #pragma unroll
     for (int j = 0; j < EPL; ++j) taken[j] = false;
-    int sel_e = -1;
     for (int q = 0; q < K; ++q) {
       uint64_t bk = 0;
       int be = 0x7fffffff;
@@ -373,7 +508,11 @@ select_warp_kernel(SelectArgs a) {
       for (int j = 0; j < EPL; ++j)
         if (be == lane * EPL + j) taken[j] = true;
       if (lane == q) sel_e = (be == 0x7fffffff) ? -1 : be;
-      if (lane == 0 && be != 0x7fffffff) atomicAdd(&cnt_s[be], 1);
+    }
+    }  // fp64 decision
+    for (int q = 0; q < K; ++q) {
+      const int eq = __shfl_sync(0xffffffffu, sel_e, q);
+      if (lane == 0 && eq >= 0) atomicAdd(&cnt_s[eq], 1);
     }
     // gates from the picked logits
     float l_sel = (lane < K && sel_e >= 0) ? load_logit(a, u, sel_e) : 0.f;

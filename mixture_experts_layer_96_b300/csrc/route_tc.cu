@@ -19,7 +19,7 @@
 namespace moe {
 
 constexpr int kRtBM = 128, kRtBK = 64, kRtThreads = 128, kRtMaxStages = 8;
-constexpr size_t kRtSmemBudget = 200 * 1024;
+constexpr size_t kRtSmemBudget = 100 * 1024;  // two CTAs per SM
 
 struct RouterTcParams {
   int64_t Tu;
@@ -228,6 +228,7 @@ cudaError_t launch_router_tc(const Problem& p, const void* x, const void* w_rout
   g.part_stride = p.Tu * p.E;
   g.stage_bytes = (uint32_t)(kRtBM * kRtBK * 2 + r.N * kRtBK * 2);
   int stages = (int)(kRtSmemBudget / g.stage_bytes);
+  if (stages < 3) stages = 3;
   g.stages = stages > kRtMaxStages ? kRtMaxStages : stages;
   g.status = status;
   const size_t smem = (size_t)g.stages * g.stage_bytes + 1024;
@@ -236,7 +237,7 @@ cudaError_t launch_router_tc(const Problem& p, const void* x, const void* w_rout
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(router_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kRtSmemBudget + 1024));
+                                         (int)(3 * (kRtBM * kRtBK * 2 + 256 * kRtBK * 2) + 1024));
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
