@@ -32,6 +32,9 @@ SMALL = [
     scaled(WORKLOADS["multihead_bf16"], T=600, h=1024, d_ff=512),
     MoEShape("drop_heavy", T=500, h=128, E=4, K=2, d_ff=128, capacity_factor=0.3, logit_bias="zipf1.2"),
     MoEShape("one_unit", T=1, h=64, E=8, K=2, d_ff=64),
+    # Switch-style top-1 routing with HAI-LLM's training / validation capacity factors
+    MoEShape("switch_top1_cf1.2", T=1000, h=256, E=16, K=1, d_ff=256, capacity_factor=1.2, logit_bias="zipf1.2"),
+    MoEShape("switch_top1_cf1.5", T=1000, h=256, E=16, K=1, d_ff=256, capacity_factor=1.5, logit_bias="zipf1.2"),
     MoEShape("dense_e1", T=200, h=64, E=1, K=1, d_ff=96),
 ]
 
