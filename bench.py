@@ -323,6 +323,21 @@ def run_ours(args, shape):
     aux = float(outs.aux.item())
     counts = outs.counts.cpu().tolist()
 
+    # kernels one forward launches (counted by the library)
+    c0 = launch_count()
+    moe_forward(cfg, x, lw, ws=ws, y=y, outputs=outs)
+    per_forward = launch_count() - c0
+    graph = None
+    if args.graph:
+        # the forward allocates and synchronises nothing, so it can be captured once and replayed
+        torch.cuda.synchronize(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            moe_forward(cfg, x, lw, ws=ws, y=y, outputs=outs)
+        graph.replay()
+        torch.cuda.synchronize(device)
+        ws.check()
+
     # ---- timed: whole forward, one event pair per step, L2 flushed between steps (untimed)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
@@ -331,11 +346,14 @@ def run_ours(args, shape):
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
-        moe_forward(cfg, x, lw, ws=ws, y=y, outputs=outs)
+        if graph is not None:
+            graph.replay()
+        else:
+            moe_forward(cfg, x, lw, ws=ws, y=y, outputs=outs)
         ev[i][1].record(stream)
     barrier()
     t1 = time.time()
-    n_launch = launch_count() - n0
+    n_launch = (per_forward * args.steps) if graph is not None else (launch_count() - n0)
     ms = aggregate_max(sum(a.elapsed_time(b) for a, b in ev) / args.steps, world, device)
     ws.check()
 
@@ -448,7 +466,8 @@ def run_ours(args, shape):
         "config": {"workload": shape.describe(), "global_batch": shape.T * world, "units_per_gpu": shape.T_units,
                    "parallelism": f"replicas x{world} (data parallel, no collective on the data path)",
                    "l2": "flushed between timed steps (512 MiB write, outside the events)",
-                   "kept_rows": kept, "aux_loss": aux, "max_over_mean_load": max(counts) / (sum(counts) / len(counts))},
+                   "kept_rows": kept, "aux_loss": aux,
+                   "cuda_graph": bool(args.graph), "kernels_per_forward": per_forward, "max_over_mean_load": max(counts) / (sum(counts) / len(counts))},
         "roofline": {"bound": "tensor", "kernel": "expert grouped GEMMs (gate/up+SwiGLU and down, 2 launches per forward)",
                      "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved_tf / peak_tf,
                      "peak_kind": peak_kind,
@@ -484,6 +503,9 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=4096, help="units the CPU-baseline oracle computes (capped at the batch)")
     ap.add_argument("--ref-sample", type=int, default=32, help="units per reference-arm step (about 0.5 s each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", dest="graph", action="store_true", default=True,
+                    help="replay the forward from a CUDA graph in the timed loop (default)")
+    ap.add_argument("--no-graph", dest="graph", action="store_false")
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
                     help="keep warming up at least this long (steady clocks); 0 for profiling runs")
     args = ap.parse_args()

@@ -105,6 +105,29 @@ def test_forward_is_deterministic_and_equals_the_stages():
     assert torch.equal(y1.view(torch.int16), y3.view(torch.int16))
 
 
+def test_forward_replays_from_a_cuda_graph():
+    """moe_forward allocates and synchronises nothing, so a captured forward replays to the same
+    bits as a direct call (the benchmark times graph replays)."""
+    shape = scaled(WORKLOADS["multihead_bf16"], T=600, h=1024, d_ff=512)
+    inp = Inputs.make(shape)
+    cfg = config_of(shape)
+    x, lw = inp.device()
+    ws = Workspace(cfg)
+    y_direct = moe_forward(cfg, x, lw, ws=ws)
+    y = torch.empty_like(y_direct)
+    outs = ForwardOutputs.allocate(cfg, "cuda")
+    moe_forward(cfg, x, lw, ws=ws, y=y, outputs=outs)  # first use outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe_forward(cfg, x, lw, ws=ws, y=y, outputs=outs)
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    ws.check()
+    assert torch.equal(y.view(torch.int16), y_direct.view(torch.int16))
+
+
 def test_forward_empty_batch():
     shape = MoEShape("empty", T=0, h=128, E=8, K=2, d_ff=128)
     cfg = config_of(shape)
