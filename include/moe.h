@@ -60,7 +60,7 @@ typedef struct CUstream_st* moe_stream_t;
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,   /* a config field or pointer is invalid; nothing was enqueued     */
-  MOE_ERR_UNSUPPORTED = 2,   /* valid for the method but not for this build (e.g. E > 256)     */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid for the method but not for this library (e.g. E > 256)   */
   MOE_ERR_WORKSPACE = 3,     /* ws is NULL or not 256-byte aligned                             */
   MOE_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed                     */
   MOE_ERR_DEVICE_STATUS = 5, /* a kernel found bad data (index/offsets out of range)            */

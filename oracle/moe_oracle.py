@@ -7,7 +7,7 @@ shares no code with it: this file imports numpy and nothing of the CUDA library.
 It is a plain, slow, obviously correct restatement of what the layer computes, in float64, with
 no blocking, fusion or reordering beyond the definitions below. Sources, by page title and section:
 
-  [L10]   "第 10 课：专家并行 EP" (Lesson 10: Expert Parallelism):
+  [Lesson 10] "第 10 课：专家并行 EP" (Lesson 10: Expert Parallelism):
           §1 (router x·W_g; s(x) = Softmax(TopK(x·W_g, K)) or sigmoid; y = Σ_{i∈TopK} s_i(x)·FFN_i(x)),
           §3 (pack per expert, local grouped GEMM, return to source order, gate-weighted sum;
               communication volume 2·Tokens·K·h·sizeof(dtype)),
@@ -62,11 +62,11 @@ def widen(a: np.ndarray, bf16: bool) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------------------------
-# [L10 §1] router
+# [Lesson 10 §1] router
 
 
 def router_logits(x: np.ndarray, w_g: np.ndarray, logit_bias: Optional[np.ndarray] = None) -> np.ndarray:
-    """l = x·W_g (+ per-expert logit bias), float64.  [L10 §1: x ∈ R^h, affinity x·W_g]
+    """l = x·W_g (+ per-expert logit bias), float64.  [Lesson 10 §1: x ∈ R^h, affinity x·W_g]
 
     x: [T'][h'] float64, w_g: [h'][E] float64 → [T'][E].
     """
@@ -89,7 +89,7 @@ def sigmoid(z: np.ndarray) -> np.ndarray:
 
 
 def selection_keys(l: np.ndarray, score: str, select_bias: Optional[np.ndarray] = None) -> np.ndarray:
-    """Keys that Top-K ranks, float64.  [L10 §1; CH10 §4; R1, R2]
+    """Keys that Top-K ranks, float64.  [Lesson 10 §1; CH10 §4; R1, R2]
 
     softmax: TopK acts on x·W_g itself, so the key is the logit.
     sigmoid: key = σ(l) + b, b the selection-only bias (zero if absent).
@@ -106,11 +106,11 @@ def selection_keys(l: np.ndarray, score: str, select_bias: Optional[np.ndarray] 
 
 
 # ---------------------------------------------------------------------------------------------
-# [L10 §5] group limit, [L10 §1] Top-K
+# [Lesson 10 §5] group limit, [Lesson 10 §1] Top-K
 
 
 def group_limit(keys: np.ndarray, n_groups: int, topk_groups: int) -> np.ndarray:
-    """Eligibility mask [T'][E] of the experts in each unit's topk_groups best groups.  [L10 §5; R3, R4]
+    """Eligibility mask [T'][E] of the experts in each unit's topk_groups best groups.  [Lesson 10 §5; R3, R4]
 
     Groups are contiguous blocks of E/n_groups experts. A group's score is the sum of its two
     largest keys (its one key if the group has a single expert).
@@ -131,7 +131,7 @@ def group_limit(keys: np.ndarray, n_groups: int, topk_groups: int) -> np.ndarray
 
 
 def topk(keys: np.ndarray, K: int, eligible: Optional[np.ndarray] = None) -> np.ndarray:
-    """Indices [T'][K] int32 of the K largest eligible keys, in (key desc, index asc) order.  [L10 §1; R4]"""
+    """Indices [T'][K] int32 of the K largest eligible keys, in (key desc, index asc) order.  [Lesson 10 §1; R4]"""
     T, E = keys.shape
     if np.isnan(keys).any():
         raise ValueError("NaN key")
@@ -147,7 +147,7 @@ def topk(keys: np.ndarray, K: int, eligible: Optional[np.ndarray] = None) -> np.
 
 
 def gates(l: np.ndarray, idx: np.ndarray, score: str) -> np.ndarray:
-    """Gate weights [T'][K] float64 of the picked experts.  [L10 §1; R1, R2]
+    """Gate weights [T'][K] float64 of the picked experts.  [Lesson 10 §1; R1, R2]
 
     softmax: Softmax(TopK(l, K)) — softmax over the K picked logits.
     sigmoid: σ(l_i) / Σ_{j picked} σ(l_j), unbiased scores.
@@ -161,7 +161,7 @@ def gates(l: np.ndarray, idx: np.ndarray, score: str) -> np.ndarray:
 
 
 def route(l: np.ndarray, score: str, K: int, select_bias=None, n_groups: int = 1, topk_groups: int = 1):
-    """(idx [T'][K] int32, gate [T'][K] float64, keys [T'][E]) from logits.  [L10 §1, §5]"""
+    """(idx [T'][K] int32, gate [T'][K] float64, keys [T'][E]) from logits.  [Lesson 10 §1, §5]"""
     keys = selection_keys(l, score, select_bias)
     elig = group_limit(keys, n_groups, topk_groups)
     idx = topk(keys, K, elig)
@@ -169,7 +169,7 @@ def route(l: np.ndarray, score: str, K: int, select_bias=None, n_groups: int = 1
 
 
 # ---------------------------------------------------------------------------------------------
-# [L10 §4] aux loss and capacity
+# [Lesson 10 §4] aux loss and capacity
 
 
 def expert_counts(idx: np.ndarray, E: int) -> np.ndarray:
@@ -178,7 +178,7 @@ def expert_counts(idx: np.ndarray, E: int) -> np.ndarray:
 
 
 def routing_probs(l: np.ndarray, score: str) -> np.ndarray:
-    """Per-unit probabilities over all E experts, float64.  [L10 §4: P_i; R7]"""
+    """Per-unit probabilities over all E experts, float64.  [Lesson 10 §4: P_i; R7]"""
     l = np.asarray(l, np.float64)
     if score == "softmax":
         z = np.exp(l - l.max(axis=1, keepdims=True))
@@ -188,7 +188,7 @@ def routing_probs(l: np.ndarray, score: str) -> np.ndarray:
 
 
 def aux_loss(l: np.ndarray, idx: np.ndarray, E: int, K: int, alpha: float, score: str) -> float:
-    """L_aux = α·E·Σ_i f_i·P_i.  [L10 §4; HAI alpha=0.01; R7]
+    """L_aux = α·E·Σ_i f_i·P_i.  [Lesson 10 §4; HAI alpha=0.01; R7]
 
     f_i = count_i/(T'·K) from the pre-drop picks; P_i = mean over units of the unit's probability
     of expert i.
@@ -200,14 +200,14 @@ def aux_loss(l: np.ndarray, idx: np.ndarray, E: int, K: int, alpha: float, score
 
 
 def capacity(capacity_factor: Optional[float], K: int, T_units: int, E: int) -> Optional[int]:
-    """C = ceil(CF·K·T'/E), or None for no drop.  [L10 §4; R5]"""
+    """C = ceil(CF·K·T'/E), or None for no drop.  [Lesson 10 §4; R5]"""
     if capacity_factor is None or not (capacity_factor > 0) or math.isinf(capacity_factor):
         return None
     return int(math.ceil(float(capacity_factor) * K * T_units / E))
 
 
 # ---------------------------------------------------------------------------------------------
-# [L10 §3 step 1] dispatch: pack units per expert, with the capacity drop of [L10 §4]
+# [Lesson 10 §3 step 1] dispatch: pack units per expert, with the capacity drop of [Lesson 10 §4]
 
 
 @dataclass
@@ -220,7 +220,7 @@ class Dispatch:
 
 
 def dispatch(idx: np.ndarray, E: int, C: Optional[int]) -> Dispatch:
-    """Per-expert queues in token order; picks past the capacity are dropped.  [L10 §3, §4; R6]
+    """Per-expert queues in token order; picks past the capacity are dropped.  [Lesson 10 §3, §4; R6]
 
     A sequential walk: units in order t = 0..T'-1, each unit's picks k = 0..K-1; the pick takes the
     next place in its expert's queue and is kept if that place is < C.
@@ -250,12 +250,12 @@ def dispatch(idx: np.ndarray, E: int, C: Optional[int]) -> Dispatch:
 
 
 def comm_volume_bytes(tokens: int, K: int, h: int, sizeof: int) -> int:
-    """Bytes moved by dispatch + combine of one layer step: 2·Tokens·K·h·sizeof.  [L10 §3]"""
+    """Bytes moved by dispatch + combine of one layer step: 2·Tokens·K·h·sizeof.  [Lesson 10 §3]"""
     return 2 * tokens * K * h * sizeof
 
 
 # ---------------------------------------------------------------------------------------------
-# [L10 §3 step 2] expert FFN (SwiGLU, R8)
+# [Lesson 10 §3 step 2] expert FFN (SwiGLU, R8)
 
 
 def silu(z: np.ndarray) -> np.ndarray:
@@ -264,7 +264,7 @@ def silu(z: np.ndarray) -> np.ndarray:
 
 
 def expert_ffn(xe: np.ndarray, w1: np.ndarray, w3: np.ndarray, w2: np.ndarray) -> np.ndarray:
-    """FFN_e(x) = W2·(silu(W1·x) ⊙ W3·x) for rows xe [n][h'], float64.  [L10 §1 FFN_i; R8]
+    """FFN_e(x) = W2·(silu(W1·x) ⊙ W3·x) for rows xe [n][h'], float64.  [Lesson 10 §1 FFN_i; R8]
 
     w1, w3: [d_ff][h']; w2: [h'][d_ff].
     """
@@ -272,11 +272,11 @@ def expert_ffn(xe: np.ndarray, w1: np.ndarray, w3: np.ndarray, w2: np.ndarray) -
 
 
 # ---------------------------------------------------------------------------------------------
-# [L10 §3 steps 3-4] combine
+# [Lesson 10 §3 steps 3-4] combine
 
 
 def combine(y_packed: np.ndarray, slot_of: np.ndarray, gate: np.ndarray) -> np.ndarray:
-    """y[t] = Σ_k gate[t,k]·y_packed[slot_of[t,k]] over kept picks.  [L10 §1 y = Σ s_i·FFN_i; §3 step 4]"""
+    """y[t] = Σ_k gate[t,k]·y_packed[slot_of[t,k]] over kept picks.  [Lesson 10 §1 y = Σ s_i·FFN_i; §3 step 4]"""
     T, K = slot_of.shape
     y = np.zeros((T, y_packed.shape[1]), dtype=np.float64)
     for k in range(K):
@@ -327,7 +327,7 @@ def forward(x: np.ndarray, w_g: np.ndarray, experts: ExpertProvider, *, E: int, 
             logit_bias=None, select_bias=None, sample_units: Optional[np.ndarray] = None,
             idx_override: Optional[np.ndarray] = None) -> Result:
     """The layer: router → scores → (group limit) → Top-K → gates → capacity drop → pack →
-    expert SwiGLU → gate-weighted combine back to token order, plus the aux loss.  [L10 §1, §3, §4, §5; MHL]
+    expert SwiGLU → gate-weighted combine back to token order, plus the aux loss.  [Lesson 10 §1, §3, §4, §5; MHL]
 
     x: [T][h] float64; w_g: [h'][E] float64; experts(e) gives expert e's float64 weights.
     sample_units: compute y only for these units (the routing and the queues still cover all
@@ -374,16 +374,16 @@ def forward(x: np.ndarray, w_g: np.ndarray, experts: ExpertProvider, *, E: int, 
 
 
 # ---------------------------------------------------------------------------------------------
-# [L10 worked example and exercise] load reporting
+# [Lesson 10 worked example and exercise] load reporting
 
 
 def expert_to_rank(num_experts: int, experts_per_rank: int) -> dict:
-    """Rank r holds experts [r·epr, (r+1)·epr).  [L10 exercise]"""
+    """Rank r holds experts [r·epr, (r+1)·epr).  [Lesson 10 exercise]"""
     return {e: e // experts_per_rank for e in range(num_experts)}
 
 
 def load_per_rank(tokens_per_expert, experts_per_rank: int) -> list:
-    """Per-rank load = tokens received by the rank's experts.  [L10 exercise]"""
+    """Per-rank load = tokens received by the rank's experts.  [Lesson 10 exercise]"""
     n = len(tokens_per_expert)
     loads = [0] * (n // experts_per_rank)
     m = expert_to_rank(n, experts_per_rank)
@@ -393,7 +393,7 @@ def load_per_rank(tokens_per_expert, experts_per_rank: int) -> list:
 
 
 def imbalance(loads) -> float:
-    """max load / mean load.  [L10 worked example]"""
+    """max load / mean load.  [Lesson 10 worked example]"""
     loads = list(loads)
     if not loads or sum(loads) == 0:
         raise ValueError("loads must be non-empty with a positive total")
@@ -401,11 +401,11 @@ def imbalance(loads) -> float:
 
 
 def routing_volume(tokens_per_expert) -> int:
-    """Routed tokens of one forward (upper bound of the all-to-all volume in tokens).  [L10 exercise]"""
+    """Routed tokens of one forward (upper bound of the all-to-all volume in tokens).  [Lesson 10 exercise]"""
     return int(sum(tokens_per_expert))
 
 
 def utilisation(loads) -> float:
-    """Σ load / (ranks · max load): useful share of the step when the slowest rank sets it.  [L10 worked example]"""
+    """Σ load / (ranks · max load): useful share of the step when the slowest rank sets it.  [Lesson 10 worked example]"""
     loads = list(loads)
     return sum(loads) / (len(loads) * max(loads))
