@@ -41,6 +41,7 @@ struct TcParams {
   int64_t rows_cap;        // packed-row capacity
   __nv_bfloat16* out;
   uint32_t* status;
+  int swap_max;            // pair tiles: last m-tiles of at most this many rows run transposed (0: none)
 };
 
 template <int EPI>
@@ -255,20 +256,47 @@ expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
 //   empty[s]  both: the MMA commit multicasts to both CTAs when the stage's MMAs are done
 //   tfull[a]  both: MMA commit multicast when accumulator a is complete
 //   tempty[a] CTA 0 only: 4 epilogue warps of each CTA arrive (remote arrive from CTA 1)
+//
+// Ragged tails. An expert's last m-tile usually holds fewer than 256 rows, and a 256-row tile
+// spends its MMAs on the missing rows as well (about a tenth of the work of a layer with ~1000
+// rows per expert). A tail of at most kSwapMaxRows rows is therefore computed transposed,
+// Dᵀ = W·Xᵀ: the 256 weight rows of the tile are the M operand and the tail's tokens, rounded up
+// to a multiple of 16, are the N operand (M = 256 allows any N that is a multiple of 16), so at
+// most 15 padding rows are computed. Operands keep their shared-memory slots (slot 0 = M operand,
+// slot 1 = N operand): in a swapped tile slot 0 holds weights and slot 1 holds token rows, CTA r
+// the tokens [r·N/2, (r+1)·N/2) of the tail. TMEM lane = output column, TMEM column = token.
+// For gate/up the 128 weight rows of CTA r are the W1 rows of output columns r·64 + [0,64) and
+// then the W3 rows of the same columns (two 64-row TMA boxes), so TMEM lanes 0-63 hold gate and
+// lanes 64-127 up. An epilogue warp reads only its own 32-lane quarter of TMEM, so the gate warp of
+// 32 columns (quarter q < 2) and the up warp of the same columns (quarter q + 2) swap half of each
+// 32-token chunk through shared memory, synchronised by an mbarrier per warp pair and buffer.
 constexpr int kPairBM = 256, kPairStages = 6;
+constexpr int kSwapMaxRows = 224;   // larger tails gain little and use the plain epilogue
+// A transposed gate/up tile's epilogue (exchange between warps, more chunks) only hides behind the
+// next tile's main loop when that is long enough; with fewer k-blocks the tails stay 256-row tiles.
+constexpr int kSwapMinKBlocks = 16;
 constexpr int kPairHalf = 128 * kBK * 2;                 // 16 KB: 128 rows x 64 bf16
 constexpr int kPairStageBytes = 2 * kPairHalf;           // A half + B half per CTA
 constexpr size_t kPairSmem = (size_t)kPairStages * kPairStageBytes + 1024;
 constexpr uint32_t kIdescPair = idesc_bf16_f32(kPairBM, kBN);
+constexpr int kSwapHalf = 64;       // W1 (then W3) rows per CTA in a swapped gate/up tile
+
+// Tokens per CTA in a swapped tail tile of `tail` rows (N = twice this, a multiple of 16).
+__device__ __forceinline__ int swap_half_n(int tail) { return ((tail + 15) & ~15) >> 1; }
 
 template <int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
 expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                           const __grid_constant__ CUtensorMap tmB1, TcParams p) {
+                           const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmS0,
+                           const __grid_constant__ CUtensorMap tmS1, TcParams p) {
   extern __shared__ unsigned char smem_dyn[];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_pre[kMaxExperts + 1];
-  __shared__ __align__(8) uint64_t s_bar[2 * kPairStages + 5];
+  __shared__ __align__(8) uint64_t s_bar[2 * kPairStages + 5 + 4];
+  // gate/up ↔ exchange of swapped tiles: [buffer][warp pair][direction: 0 gate→up, 1 up→gate][token][lane]
+  __shared__ __align__(16) float s_xch[EPI == kEpiSwiGLU ? 2 * 2 * 2 * 16 * 32 : 1];
+  // swapped tiles: per epilogue warp, a [token][32 columns] bf16 chunk turned into row-vector stores
+  __shared__ __align__(16) __nv_bfloat16 s_stage[4 * 32 * 32];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_ok;
@@ -283,6 +311,7 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kPairStages + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kPairStages + 2 + a); };
   const uint32_t done_bar = bar0 + 8u * (2 * kPairStages + 4);
+  auto xch_bar = [&](int pair, int buf) { return bar0 + 8u * (2 * kPairStages + 5 + 2 * pair + buf); };
 
   if (warp == 0) {
     const bool ok = warp_tile_prefix(p.offsets, p.E, kPairBM, p.rows_cap, s_off, s_pre);
@@ -299,10 +328,15 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
         mbar_init(tempty_bar(a), 8);
       }
       mbar_init(done_bar, 1);
+      for (int b = 0; b < 4; ++b) mbar_init(xch_bar(b >> 1, b & 1), 64);  // both warps' lanes
       fence_mbar_init();
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB0);
-      if (EPI == kEpiSwiGLU) tma_prefetch_desc(&tmB1);
+      if (EPI == kEpiSwiGLU) {
+        tma_prefetch_desc(&tmB1);
+        tma_prefetch_desc(&tmS0);
+        tma_prefetch_desc(&tmS1);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -336,16 +370,31 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
       for (int tile = cid; tile < total && !aborted; tile += ncl) {
         int e, mt, nt;
         decode_tile(tile, s_pre, p.E, p.n_tiles, e, mt, nt);
-        const int a_row = s_off[e] + mt * kPairBM + (int)rank * 128;
+        const int tail = s_off[e + 1] - s_off[e] - mt * kPairBM;
+        const bool swap = tail <= p.swap_max;
+        const int a_row = s_off[e] + mt * kPairBM + (int)rank * (swap ? swap_half_n(tail) : 128);
         const int b_row = (EPI == kEpiSwiGLU) ? e * p.w_rows + nt * (kBN / 2)
                                               : e * p.w_rows + nt * kBN + (int)rank * 128;
+        // swapped gate/up: first W1/W3 row of this CTA's 64 output columns
+        const int s_row = e * p.w_rows + nt * (kBN / 2) + (int)rank * kSwapHalf;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { aborted = true; break; }
           const uint32_t sa = sbase + stage * kPairStageBytes;
           if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * kPairStageBytes);
           const uint32_t fb = full0_leader + 8u * stage;
-          tma_load_2d_pair(sa, &tmA, fb, kb * kBK, a_row);
-          tma_load_2d_pair(sa + kPairHalf, mb, fb, kb * kBK, b_row);
+          if (!swap) {
+            tma_load_2d_pair(sa, &tmA, fb, kb * kBK, a_row);
+            tma_load_2d_pair(sa + kPairHalf, mb, fb, kb * kBK, b_row);
+          } else {
+            // token rows into slot 1 (the MMA reads the first N/2 of the 128 loaded)
+            tma_load_2d_pair(sa + kPairHalf, &tmA, fb, kb * kBK, a_row);
+            if (EPI == kEpiSwiGLU) {
+              tma_load_2d_pair(sa, &tmS0, fb, kb * kBK, s_row);
+              tma_load_2d_pair(sa + kSwapHalf * kBK * 2, &tmS1, fb, kb * kBK, s_row);
+            } else {
+              tma_load_2d_pair(sa, mb, fb, kb * kBK, b_row);
+            }
+          }
           filled |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
@@ -377,6 +426,11 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) { aborted = true; break; }
         tc_fence_after();
+        int e, mt, nt;
+        decode_tile(tile, s_pre, p.E, p.n_tiles, e, mt, nt);
+        const int tail = s_off[e + 1] - s_off[e] - mt * kPairBM;
+        const uint32_t idesc =
+            tail <= p.swap_max ? idesc_bf16_f32(kPairBM, 2 * swap_half_n(tail)) : kIdescPair;
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag)) { aborted = true; break; }
@@ -385,7 +439,7 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
           const uint64_t ad = sdesc_kmajor_sw128(sa), bd = sdesc_kmajor_sw128(sa + kPairHalf);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            umma_bf16_pair(d_tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), kIdescPair,
+            umma_bf16_pair(d_tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
                            (kb > 0 || k > 0) ? 1u : 0u);
           umma_commit_pair_mc(empty_bar(stage), (uint16_t)0x3);
           if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
@@ -403,7 +457,9 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
     const int q = warp & 3;
     const uint32_t tempty_leader0 = mapa_shared(tempty_bar(0), 0);
     int it = 0;
-    for (int tile = cid; tile < total; tile += ncl, ++it) {
+    uint32_t xn = 0;     // exchange chunks done by this warp (its partner does the same sequence)
+    bool failed = false;
+    for (int tile = cid; tile < total && !failed; tile += ncl, ++it) {
       int e, mt, nt;
       decode_tile(tile, s_pre, p.E, p.n_tiles, e, mt, nt);
       const int acc = it & 1;
@@ -414,11 +470,85 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
       }
       tc_fence_after();
       const int rows_e = s_off[e + 1] - s_off[e];
+      const int tail = rows_e - mt * kPairBM;
       const int r_local = mt * kPairBM + (int)rank * 128 + q * 32 + lane;
       const bool row_ok = r_local < rows_e;
       __nv_bfloat16* orow = p.out + (int64_t)(s_off[e] + r_local) * p.n_out;
       const uint32_t t_row = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(q * 32) << 16);
-      if (EPI == kEpiSwiGLU) {
+      if (tail <= p.swap_max) {
+        // transposed tile: lane = output column, TMEM column = token of the tail. Each warp puts a
+        // chunk of [tokens][its 32 columns] in bf16 into its staging area, then writes it out as
+        // 16-byte pieces of output rows (four per token: 32 columns = 64 bytes).
+        const int n_tok = 2 * swap_half_n(tail);
+        __nv_bfloat16* obase = p.out + (int64_t)(s_off[e] + mt * kPairBM) * p.n_out;
+        __nv_bfloat16* stg = s_stage + (warp - 2) * 32 * 32;
+        if (EPI == kEpiSwiGLU) {
+          // quarter q < 2: gate of columns 32q + lane; quarter q + 2: up of the same columns. The
+          // gate warp finishes tokens c0..c0+15 of each chunk, the up warp c0+16..c0+31.
+          const bool gate_warp = q < 2;
+          const int wp = q & 1;
+          const int col0 = nt * 128 + (int)rank * kSwapHalf + wp * 32;
+          const bool cols_ok = col0 < p.n_out;  // n_out is a multiple of 32
+#pragma unroll 1
+          for (int c0 = 0; c0 < n_tok; c0 += 32, ++xn) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(t_row + c0, v);
+            tmem_ld_wait();
+            const int buf = (int)(xn & 1u);
+            float* xb = s_xch + (size_t)((buf * 2 + wp) * 2) * 16 * 32;
+            float* mine = xb + (gate_warp ? 0 : 16 * 32);       // what this warp hands over
+            const float* theirs = xb + (gate_warp ? 16 * 32 : 0);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mine[i * 32 + lane] = __uint_as_float(gate_warp ? v[16 + i] : v[i]);
+            mbar_arrive(xch_bar(wp, buf));
+            if (!mbar_wait(xch_bar(wp, buf), (xn >> 1) & 1u, abort_flag)) {
+              failed = true;
+              break;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float other = theirs[i * 32 + lane];
+              const float g = gate_warp ? __uint_as_float(v[i]) : other;
+              const float u = gate_warp ? other : __uint_as_float(v[16 + i]);
+              stg[i * 32 + lane] = __float2bfloat16_rn(silu_f32(g) * u);
+            }
+            __syncwarp();
+            const int t0 = c0 + (gate_warp ? 0 : 16);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int j = lane + 32 * k, t = j >> 2, part = j & 3;
+              if (cols_ok && t0 + t < tail)
+                *reinterpret_cast<uint4*>(obase + (int64_t)(t0 + t) * p.n_out + col0 + part * 8) =
+                    *reinterpret_cast<const uint4*>(stg + t * 32 + part * 8);
+            }
+            __syncwarp();
+          }
+          if (failed) {
+            if (lane == 0) abort_both();
+            break;
+          }
+        } else {
+          const int col0 = nt * kBN + (int)rank * 128 + q * 32;
+          const bool cols_ok = col0 < p.n_out;
+#pragma unroll 1
+          for (int c0 = 0; c0 < n_tok; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(t_row + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) stg[i * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[i]));
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int j = lane + 32 * k, t = j >> 2, part = j & 3;
+              if (cols_ok && c0 + t < tail)
+                *reinterpret_cast<uint4*>(obase + (int64_t)(c0 + t) * p.n_out + col0 + part * 8) =
+                    *reinterpret_cast<const uint4*>(stg + t * 32 + part * 8);
+            }
+            __syncwarp();
+          }
+        }
+      } else if (EPI == kEpiSwiGLU) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t g[32], u[32];
@@ -473,19 +603,40 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
   }
 }
 
+// The kernels are persistent: a cluster that could not be resident alongside the others would run
+// its whole share of tiles after them. The grid is capped at the clusters the GPU holds at once
+// (asked once per device).
+template <typename Kern>
+static int resident_cluster_grid(Kern kern, int cluster, size_t smem, int want) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)want);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    return want;
+  }
+  return n * cluster < want ? n * cluster : want;
+}
+
 template <int EPI>
 static cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                                  const TcParams& p, int grid, cudaStream_t s) {
+                                  const CUtensorMap& s0, const CUtensorMap& s1, const TcParams& p,
+                                  int grid, cudaStream_t s) {
   static bool attr_done[64] = {false};
+  static int grid_cap[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(expert_gemm_tc_pair_kernel<EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmem);
     if (e != cudaSuccess) return e;
+    grid_cap[dev] = resident_cluster_grid(expert_gemm_tc_pair_kernel<EPI>, 2, kPairSmem, grid);
     attr_done[dev] = true;
   }
-  expert_gemm_tc_pair_kernel<EPI><<<grid, kTcThreads, kPairSmem, s>>>(a, b0, b1, p);
+  if (dev < 64 && grid_cap[dev] > 0 && grid > grid_cap[dev]) grid = grid_cap[dev];
+  expert_gemm_tc_pair_kernel<EPI><<<grid, kTcThreads, kPairSmem, s>>>(a, b0, b1, s0, s1, p);
   note_launch();
   return cudaGetLastError();
 }
@@ -496,6 +647,14 @@ static bool use_pair_tiles(const Problem& p) {
   const char* v = getenv("MOE_TC_PAIR");
   if (v && (v[0] == '0' || v[0] == '1') && v[1] == 0) return v[0] == '1';
   return p.rows / p.E >= kPairBM;
+}
+
+// Largest tail (rows) that a pair-tile GEMM with reduction length K runs transposed.
+// MOE_TC_SWAP=0/1 forces the transposed tails off/on whatever K is.
+static int swap_max_rows(int K) {
+  const char* v = getenv("MOE_TC_SWAP");
+  if (v && (v[0] == '0' || v[0] == '1') && v[1] == 0) return v[0] == '1' ? kSwapMaxRows : 0;
+  return (K + kBK - 1) / kBK >= kSwapMinKBlocks ? kSwapMaxRows : 0;
 }
 
 template <int EPI>
@@ -534,8 +693,10 @@ cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int3
       !encode_tmap_2d_bf16(&mW2, w_down, (uint64_t)p.d_ff, (uint64_t)p.E * p.hu, kBK, kBN))
     return cudaErrorInvalidValue;
   const bool pair = use_pair_tiles(p);
-  CUtensorMap mW2p;
-  if (pair && !encode_tmap_2d_bf16(&mW2p, w_down, (uint64_t)p.d_ff, (uint64_t)p.E * p.hu, kBK, kBN / 2))
+  CUtensorMap mW2p, mW1s, mW3s;  // pair tiles: W2 in 128-row halves; W1/W3 in 64-row halves (tails)
+  if (pair && (!encode_tmap_2d_bf16(&mW2p, w_down, (uint64_t)p.d_ff, (uint64_t)p.E * p.hu, kBK, kBN / 2) ||
+               !encode_tmap_2d_bf16(&mW1s, w_gate, (uint64_t)p.hu, (uint64_t)p.E * p.d_ff, kBK, kSwapHalf) ||
+               !encode_tmap_2d_bf16(&mW3s, w_up, (uint64_t)p.hu, (uint64_t)p.E * p.d_ff, kBK, kSwapHalf)))
     return cudaErrorInvalidValue;
   const int sms = device_sm_count();
   const int grid = pair ? (sms / 2) * 2 : sms;
@@ -550,7 +711,8 @@ cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int3
   g.n_tiles = (p.d_ff + kBN / 2 - 1) / (kBN / 2);
   g.n_out = p.d_ff;
   g.out = static_cast<__nv_bfloat16*>(hidden);
-  cudaError_t e = pair ? launch_tc_pair<kEpiSwiGLU>(mA, mW1, mW3, g, grid, s)
+  g.swap_max = swap_max_rows(g.K);
+  cudaError_t e = pair ? launch_tc_pair<kEpiSwiGLU>(mA, mW1, mW3, mW1s, mW3s, g, grid, s)
                        : launch_tc<kEpiSwiGLU>(mA, mW1, mW3, g, grid, s);
   if (e != cudaSuccess) return e;
   // down → y_packed
@@ -559,7 +721,8 @@ cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int3
   g.n_tiles = (p.hu + kBN - 1) / kBN;
   g.n_out = p.hu;
   g.out = static_cast<__nv_bfloat16*>(y_packed);
-  return pair ? launch_tc_pair<kEpiPlain>(mH, mW2p, mW2p, g, grid, s)
+  g.swap_max = swap_max_rows(g.K);
+  return pair ? launch_tc_pair<kEpiPlain>(mH, mW2p, mW2p, mW2p, mW2p, g, grid, s)
               : launch_tc<kEpiPlain>(mH, mW2, mW2, g, grid, s);
 }
 

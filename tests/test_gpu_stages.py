@@ -127,10 +127,17 @@ FFN_CASES = [
 ]
 
 
-@pytest.fixture(params=["single", "pair"])
+@pytest.fixture(params=["single", "pair", "pair_tails_transposed", "pair_tails_plain"])
 def tile_mode(request, monkeypatch):
-    """Run an expert-FFN case with the single-CTA 128-row tiles and with the CTA-pair 256-row tiles."""
-    monkeypatch.setenv("MOE_TC_PAIR", "1" if request.param == "pair" else "0")
+    """Run an expert-FFN case with the single-CTA 128-row tiles and with the CTA-pair 256-row tiles,
+    the latter with the automatic choice for experts' last m-tiles and with every tail of up to 224
+    rows forced to the transposed tile or to the 256-row tile."""
+    monkeypatch.setenv("MOE_TC_PAIR", "0" if request.param == "single" else "1")
+    swap = {"pair_tails_transposed": "1", "pair_tails_plain": "0"}.get(request.param)
+    if swap is None:
+        monkeypatch.delenv("MOE_TC_SWAP", raising=False)
+    else:
+        monkeypatch.setenv("MOE_TC_SWAP", swap)
     return request.param
 
 
@@ -184,6 +191,38 @@ def test_expert_ffn_empty_and_skewed_experts(tile_mode):
             ref[r0:r1] = O.expert_ffn(widen(xu[r0:r1], True), widen(w1[e], True), widen(w3[e], True), widen(w2[e], True))
     ok, err, bound = tol_ok(got, ref, "bf16")
     assert ok, f"max err {err} > {bound}"
+
+
+@pytest.mark.parametrize("h,d_ff", [(128, 256), (96, 160)], ids=["aligned", "ragged_widths"])
+def test_expert_ffn_ragged_tails(tile_mode, h, d_ff):
+    """Experts whose row counts put every kind of last m-tile in the batch: tails of 1, 16 and 17
+    rows, at and just past the largest transposed tail (224, 225), just short of and at a full pair
+    tile (255, 256), one row into the next (257), an expert of one full tile plus a tail (480)."""
+    sizes = [1, 16, 17, 224, 225, 255, 256, 257, 480, 0, 33]
+    E = len(sizes)
+    shape = MoEShape("tails", T=900, h=h, E=E, K=2, d_ff=d_ff)
+    cfg = config_of(shape)
+    g = Generator(shape)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    kept = int(offsets[-1])
+    xu = Generator(scaled(shape, T=shape.T_units * shape.K)).x()
+    w1, w3, w2 = g.experts()
+    ws = Workspace(cfg)
+    yp = moe_expert_ffn(cfg, to_device(xu, True), torch.from_numpy(offsets).cuda(), to_device(w1, True),
+                        to_device(w3, True), to_device(w2, True), ws=ws)
+    ws.check()
+    got = as_f64(yp)[:kept]
+    ref = np.zeros_like(got)
+    for e in range(E):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 > r0:
+            ref[r0:r1] = O.expert_ffn(widen(xu[r0:r1], True), widen(w1[e], True), widen(w3[e], True), widen(w2[e], True))
+    for e in range(E):  # per expert, so that a wrong tail shows which one
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 == r0:
+            continue
+        ok, err, bound = tol_ok(got[r0:r1], ref[r0:r1], "bf16")
+        assert ok, f"expert {e} ({sizes[e]} rows): max err {err} > {bound}"
 
 
 def test_expert_ffn_flags_bad_offsets():
