@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define MOE_API __attribute__((visibility("default")))
@@ -165,6 +165,50 @@ MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const void* y_packed, 
  * `out` may be NULL or have NULL members; intermediates live in `ws`. */
 MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
                          const moe_outputs_t* out, void* ws, moe_stream_t stream);
+
+/* ---- training: forward that keeps what the backward needs, and the backward ----------------
+ * The pages train this layer ([HAI] §"HAI-LLM 上的使用"; [Lesson 10 §4] adds L_aux to the training
+ * loss) but give no backward formulas. The backward here is the gradient of
+ *     L = <dy, y> + d_aux·L_aux
+ * with the routing held fixed: the Top-K picks, the group limit, the counts f_i and the capacity
+ * drops are piecewise constant and get no gradient; gradients flow through the gates, the expert
+ * FFNs, the probabilities P_i of L_aux and the router GEMM. The selection-only bias has none.
+ * Supported: dtype MOE_BF16 with h' and d_ff multiples of 64 (else MOE_ERR_UNSUPPORTED). */
+
+/* Bytes of the G | U buffer moe_forward_train fills: T'·K rows of 2·d_ff bf16 (host only). */
+MOE_API size_t moe_saved_gu_size(const moe_config_t* cfg);
+
+/* moe_forward, and also the SwiGLU inputs G = X_e·W1_eᵀ and U = X_e·W3_eᵀ of every kept packed
+ * row, bf16, into gu [T'·K][2·d_ff] (G in columns [0, d_ff), U in [d_ff, 2·d_ff)).
+ * `out` is required, with topk_idx, topk_gate, logits and slot_of non-NULL (the backward reads
+ * them). Keep `ws`, `out` and `gu` unchanged until moe_backward has run: the backward also reads
+ * the forward's packed rows, hidden activations and expert outputs from `ws`. */
+MOE_API moe_status_t moe_forward_train(const moe_config_t* cfg, const void* x, const moe_weights_t* w,
+                                       void* y, const moe_outputs_t* out, void* gu, void* ws,
+                                       moe_stream_t stream);
+
+/* Gradients (device pointers). dlogits and dgate may be NULL (then they stay in `bws`). */
+typedef struct {
+  void* dx;                /* [T][h] bf16: dL/dx                                                  */
+  float* dw_router;        /* [h'][E] fp32: dL/dW_g                                               */
+  float* dw_gate;          /* [E][d_ff][h'] fp32: dL/dW1                                           */
+  float* dw_up;            /* [E][d_ff][h'] fp32: dL/dW3                                           */
+  float* dw_down;          /* [E][h'][d_ff] fp32: dL/dW2                                           */
+  float* dlogits;          /* [T'][E] fp32: dL/dl (l the router logits, logit bias included)       */
+  float* dgate;            /* [T'][K] fp32: dL/d gate (0 for dropped picks)                        */
+} moe_grads_t;
+
+/* Bytes of backward scratch `bws` for this config (host only; 256-byte aligned when allocated). */
+MOE_API size_t moe_backward_workspace_size(const moe_config_t* cfg);
+
+/* Backward of the moe_forward_train call that filled `ws`, `out` and `gu` for this x and w.
+ *  dy [T][h] bf16: dL/dy. d_aux: weight of L_aux in L (host float).
+ *  Out: every member of `grads` except dlogits/dgate is required; dw_* are overwritten (not
+ *  accumulated). Deterministic: the same inputs give the same bits. Errors as for moe_forward;
+ *  kernel faults set the status word of `ws`. */
+MOE_API moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weights_t* w,
+                                  const void* dy, float d_aux, const moe_outputs_t* out, const void* gu,
+                                  void* ws, const moe_grads_t* grads, void* bws, moe_stream_t stream);
 
 /* Wait for `stream`, read and clear the status word in `ws`: MOE_OK, MOE_ERR_DEVICE_STATUS or
  * MOE_ERR_TIMEOUT (or MOE_ERR_CUDA if the wait itself failed). */

@@ -1,0 +1,279 @@
+// Backward of the layer outside the expert GEMMs (bf16 layers), with the routing held fixed:
+//   combine   y[t] = Σ_k kept g[t,k]·Y_packed[slot]      →  dY_packed[slot] = g[t,k]·dy[t],
+//                                                           dg[t,k] = <dy[t], Y_packed[slot]>
+//             [Lesson 10 "专家并行 EP", §1 y = Σ s_i·FFN_i; §3 step 4]
+//   gates     softmax over the picked logits, or σ(l_i)/Σ_picked σ(l_j)  →  dL/dl   [Lesson 10 §1]
+//   aux loss  α·E·Σ_i f_i·P_i with f fixed, P_i = mean_t p[t,i]          →  dL/dl   [Lesson 10 §4]
+//   router    l = x·W_g (+ bias)  →  dW_g = xᵀ·dl,  dx += dl·W_gᵀ                  [Lesson 10 §1]
+//   dispatch  x_packed[slot] = x[t]  →  dx[t] += Σ_k kept dX_packed[slot]           [Lesson 10 §3 step 1]
+// Every sum has a fixed order (warp butterflies, per-thread loops, chunk partials added in chunk
+// order), so the gradients are deterministic.
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = __uint_as_float(w[j] << 16);
+    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 f32x8_to_bf16(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+// One warp per unit: for each kept pick, dY_packed[slot] = g·dy[t] and dg = <dy[t], Y_packed[slot]>.
+__global__ void bwd_combine_kernel(const uint4* __restrict__ dy, const uint4* __restrict__ y_packed,
+                                   const int32_t* __restrict__ slot_of, const float* __restrict__ gate,
+                                   int64_t Tu, int K, int vecs, int64_t rows, uint4* __restrict__ dy_packed,
+                                   float* __restrict__ dgate, uint32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (u >= Tu) return;
+  const uint4* d = dy + u * vecs;
+  for (int k = 0; k < K; ++k) {
+    const int32_t slot = slot_of[u * K + k];
+    float acc = 0.0f;
+    if (slot >= 0 && slot < rows) {
+      const float g = gate[u * K + k];
+      const uint4* yp = y_packed + (int64_t)slot * vecs;
+      uint4* o = dy_packed + (int64_t)slot * vecs;
+      for (int v = lane; v < vecs; v += 32) {
+        float a[8], b[8], c[8];
+        bf16x8_to_f32(d[v], a);
+        bf16x8_to_f32(yp[v], b);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          acc = fmaf(a[j], b[j], acc);
+          c[j] = g * a[j];
+        }
+        o[v] = f32x8_to_bf16(c);
+      }
+    } else if (slot >= rows && lane == 0) {
+      set_status(status, kDevErrBadIndex);
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) dgate[u * K + k] = acc;
+  }
+}
+
+// One thread per unit: dL/dl[t][:] through the gates of its picks and through P_i of the aux loss.
+template <bool SIGMOID>
+__global__ void bwd_logits_kernel(const float* __restrict__ logits, const int32_t* __restrict__ idx,
+                                  const float* __restrict__ gate, const float* __restrict__ dgate,
+                                  const int32_t* __restrict__ counts, int64_t Tu, int E, int K, float aux_scale,
+                                  float* __restrict__ dl) {
+  const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= Tu) return;
+  const float* l = logits + u * E;
+  float* o = dl + u * E;
+  // aux: dL/dp[t,i] = aux_scale·f_i with aux_scale = d_aux·α·E/T' and f_i = counts_i/(T'·K)
+  const float f_scale = 1.0f / (float)((double)Tu * K);
+  float mx = -INFINITY;
+  if (!SIGMOID)
+    for (int e = 0; e < E; ++e) mx = fmaxf(mx, l[e]);
+  float z = 0.0f, inner = 0.0f;  // Σ_i q_i and Σ_i q_i·dp_i, q = exp(l − max) or σ(l)
+  for (int e = 0; e < E; ++e) {
+    const float q = SIGMOID ? 1.0f / (1.0f + __expf(-l[e])) : __expf(l[e] - mx);
+    const float dp = aux_scale * (float)counts[e] * f_scale;
+    z += q;
+    inner = fmaf(q, dp, inner);
+  }
+  inner /= z;  // Σ_i p_i·dp_i
+  for (int e = 0; e < E; ++e) {
+    const float dp = aux_scale * (float)counts[e] * f_scale;
+    if (SIGMOID) {
+      const float s = 1.0f / (1.0f + __expf(-l[e]));
+      o[e] = (dp - inner) / z * s * (1.0f - s);
+    } else {
+      o[e] = __expf(l[e] - mx) / z * (dp - inner);
+    }
+  }
+  // gates: softmax over the picks (dl = g ⊙ (dg − Σ g·dg)) or s/Σs (ds = (dg − Σ g·dg)/Σs)
+  float gin = 0.0f, ssum = 0.0f;
+  for (int k = 0; k < K; ++k) {
+    gin = fmaf(gate[u * K + k], dgate[u * K + k], gin);
+    if (SIGMOID) ssum += 1.0f / (1.0f + __expf(-l[idx[u * K + k]]));
+  }
+  for (int k = 0; k < K; ++k) {
+    const int e = idx[u * K + k];
+    if (e < 0 || e >= E) continue;
+    const float r = dgate[u * K + k] - gin;
+    if (SIGMOID) {
+      const float s = 1.0f / (1.0f + __expf(-l[e]));
+      o[e] += r / ssum * s * (1.0f - s);
+    } else {
+      o[e] += gate[u * K + k] * r;
+    }
+  }
+}
+
+// dW_g partials: block (i-tile of 64, e-tile of 64, token chunk) → part[chunk][i][e] = Σ_t x[t][i]·dl[t][e].
+constexpr int kWgTile = 64, kWgT = 32;
+__global__ void __launch_bounds__(256) bwd_wg_partial_kernel(const __nv_bfloat16* __restrict__ x,
+                                                             const float* __restrict__ dl, int64_t Tu, int hu,
+                                                             int E, int64_t chunk_len, float* __restrict__ part) {
+  __shared__ float sx[kWgT][kWgTile + 1];
+  __shared__ float sd[kWgT][kWgTile + 1];
+  const int i0 = blockIdx.x * kWgTile, e0 = blockIdx.y * kWgTile;
+  const int64_t t_begin = (int64_t)blockIdx.z * chunk_len;
+  const int64_t t_end = t_begin + chunk_len < Tu ? t_begin + chunk_len : Tu;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 x 16 threads, 4 x 4 outputs each
+  float acc[4][4] = {};
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += kWgT) {
+    for (int j = threadIdx.x; j < kWgT * kWgTile; j += 256) {
+      const int r = j / kWgTile, c = j % kWgTile;
+      const int64_t t = t0 + r;
+      sx[r][c] = (t < t_end && i0 + c < hu) ? __bfloat162float(x[t * hu + i0 + c]) : 0.0f;
+      sd[r][c] = (t < t_end && e0 + c < E) ? dl[t * E + e0 + c] : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int r = 0; r < kWgT; ++r) {
+      float a[4], b[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        a[j] = sx[r][ty * 4 + j];
+        b[j] = sd[r][tx * 4 + j];
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) acc[m][n] = fmaf(a[m], b[n], acc[m][n]);
+    }
+    __syncthreads();
+  }
+  float* out = part + (int64_t)blockIdx.z * hu * E;
+#pragma unroll
+  for (int m = 0; m < 4; ++m)
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      const int i = i0 + ty * 4 + m, e = e0 + tx * 4 + n;
+      if (i < hu && e < E) out[(int64_t)i * E + e] = acc[m][n];
+    }
+}
+
+__global__ void bwd_wg_reduce_kernel(const float* __restrict__ part, int nchunks, int64_t n, float* __restrict__ dwg) {
+  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= n) return;
+  float s = 0.0f;
+  for (int c = 0; c < nchunks; ++c) s += part[(int64_t)c * n + j];
+  dwg[j] = s;
+}
+
+// One warp per unit: dx[t] = Σ_k kept dX_packed[slot] + Σ_e dl[t][e]·W_gᵀ[e] (bf16 out).
+__global__ void bwd_dx_kernel(const uint4* __restrict__ dx_packed, const int32_t* __restrict__ slot_of,
+                              const float* __restrict__ dl, const uint4* __restrict__ wgt, int64_t Tu, int K,
+                              int E, int vecs, int64_t rows, uint4* __restrict__ dx) {
+  extern __shared__ float s_dl[];  // [warps][E]
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  float* my = s_dl + w * E;
+  if (u < Tu)
+    for (int e = lane; e < E; e += 32) my[e] = dl[u * E + e];
+  __syncwarp();
+  if (u >= Tu) return;
+  int32_t slots[kMaxTopK];
+#pragma unroll
+  for (int k = 0; k < kMaxTopK; ++k) slots[k] = k < K ? slot_of[u * K + k] : -1;
+  for (int v = lane; v < vecs; v += 32) {
+    float acc[8] = {};
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k) {
+      if (slots[k] >= 0 && slots[k] < rows) {
+        float f[8];
+        bf16x8_to_f32(dx_packed[(int64_t)slots[k] * vecs + v], f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] += f[j];
+      }
+    }
+    for (int e = 0; e < E; ++e) {
+      float f[8];
+      bf16x8_to_f32(wgt[(int64_t)e * vecs + v], f);
+      const float d = my[e];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = fmaf(d, f[j], acc[j]);
+    }
+    dx[u * vecs + v] = f32x8_to_bf16(acc);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_backward_misc_combine(const Problem& p, const void* dy, const void* y_packed,
+                                         const int32_t* slot_of, const float* gate, void* dy_packed,
+                                         float* dgate, uint32_t* status, cudaStream_t s) {
+  if (p.Tu == 0) return cudaSuccess;
+  const int vecs = p.hu / 8;
+  const int64_t blocks = (p.Tu * 32 + 255) / 256;
+  bwd_combine_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4*>(dy),
+                                                       static_cast<const uint4*>(y_packed), slot_of, gate,
+                                                       p.Tu, p.K, vecs, p.rows, static_cast<uint4*>(dy_packed),
+                                                       dgate, status);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_backward_logits(const Problem& p, const float* logits, const int32_t* idx, const float* gate,
+                                   const float* dgate, const int32_t* counts, float d_aux, float* dl,
+                                   cudaStream_t s) {
+  if (p.Tu == 0) return cudaSuccess;
+  const float aux_scale = (float)((double)d_aux * p.cfg.aux_alpha * p.E / (double)p.Tu);
+  const unsigned blocks = (unsigned)((p.Tu + 127) / 128);
+  if (p.sigmoid)
+    bwd_logits_kernel<true><<<blocks, 128, 0, s>>>(logits, idx, gate, dgate, counts, p.Tu, p.E, p.K, aux_scale, dl);
+  else
+    bwd_logits_kernel<false><<<blocks, 128, 0, s>>>(logits, idx, gate, dgate, counts, p.Tu, p.E, p.K, aux_scale, dl);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// Chunks of the token range for the dW_g partials: about 512 blocks (several per SM on a B300),
+// fixed by the config alone so that the backward workspace size needs no device query.
+int backward_wg_chunks(const Problem& p) {
+  const int64_t tiles = (int64_t)((p.hu + kWgTile - 1) / kWgTile) * ((p.E + kWgTile - 1) / kWgTile);
+  int64_t c = (512 + tiles - 1) / tiles;
+  const int64_t max_c = (p.Tu + kWgT - 1) / kWgT;
+  if (c > max_c) c = max_c;
+  if (c < 1) c = 1;
+  if (c > 1024) c = 1024;
+  return (int)c;
+}
+
+cudaError_t launch_backward_router(const Problem& p, const void* x, const float* dl, int nchunks, float* part,
+                                   float* dw_router, cudaStream_t s) {
+  const int64_t n = (int64_t)p.hu * p.E;
+  if (p.Tu == 0) return cudaMemsetAsync(dw_router, 0, (size_t)n * 4, s);
+  int64_t chunk_len = (p.Tu + nchunks - 1) / nchunks;
+  chunk_len = (chunk_len + kWgT - 1) / kWgT * kWgT;
+  const dim3 grid((p.hu + kWgTile - 1) / kWgTile, (p.E + kWgTile - 1) / kWgTile, (unsigned)nchunks);
+  bwd_wg_partial_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), dl, p.Tu, p.hu, p.E, chunk_len,
+                                             part);
+  note_launch();
+  bwd_wg_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(part, nchunks, n, dw_router);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_backward_dx(const Problem& p, const void* dx_packed, const int32_t* slot_of, const float* dl,
+                               const void* w_router_t, void* dx, cudaStream_t s) {
+  if (p.Tu == 0) return cudaSuccess;
+  const int vecs = p.hu / 8;
+  const int64_t blocks = (p.Tu * 32 + 255) / 256;
+  const size_t smem = (size_t)8 * p.E * sizeof(float);
+  bwd_dx_kernel<<<(unsigned)blocks, 256, smem, s>>>(static_cast<const uint4*>(dx_packed), slot_of, dl,
+                                                    static_cast<const uint4*>(w_router_t), p.Tu, p.K, p.E, vecs,
+                                                    p.rows, static_cast<uint4*>(dx));
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

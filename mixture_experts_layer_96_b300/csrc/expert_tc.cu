@@ -42,7 +42,19 @@ struct TcParams {
   __nv_bfloat16* out;
   uint32_t* status;
   int swap_max;            // pair tiles: last m-tiles of at most this many rows run transposed (0: none)
+  __nv_bfloat16* save_gu;  // gate/up: G | U pre-activations [rows][2·n_out] (bf16) when not null
 };
+
+// 32 fp32 values (as bits) → 32 bf16 at dst (64 bytes, 16-byte aligned).
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t (&v)[32]) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    d4[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
+                       pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                       pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                       pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+}
 
 template <int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -202,6 +214,11 @@ expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
           tmem_ld_wait();
           const int col = nt * 128 + c * 32;
           if (row_ok && col < p.n_out) {
+            if (p.save_gu != nullptr) {
+              __nv_bfloat16* sg = p.save_gu + (int64_t)(s_off[e] + r_local) * (2 * p.n_out) + col;
+              store_bf16x32(sg, g);
+              store_bf16x32(sg + p.n_out, u);
+            }
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -522,6 +539,29 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
                     *reinterpret_cast<const uint4*>(stg + t * 32 + part * 8);
             }
             __syncwarp();
+            if (p.save_gu != nullptr) {
+              // G, then U, of the same 16 tokens x 32 columns, through the staging area
+              __nv_bfloat16* sbase_gu = p.save_gu + (int64_t)(s_off[e] + mt * kPairBM) * (2 * p.n_out);
+#pragma unroll 1
+              for (int which = 0; which < 2; ++which) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const float other = theirs[i * 32 + lane];
+                  const float g = gate_warp ? __uint_as_float(v[i]) : other;
+                  const float u = gate_warp ? other : __uint_as_float(v[16 + i]);
+                  stg[i * 32 + lane] = __float2bfloat16_rn(which == 0 ? g : u);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  const int j = lane + 32 * k, t = j >> 2, part = j & 3;
+                  if (cols_ok && t0 + t < tail)
+                    *reinterpret_cast<uint4*>(sbase_gu + (int64_t)(t0 + t) * (2 * p.n_out) + which * p.n_out +
+                                              col0 + part * 8) = *reinterpret_cast<const uint4*>(stg + t * 32 + part * 8);
+                }
+                __syncwarp();
+              }
+            }
           }
           if (failed) {
             if (lane == 0) abort_both();
@@ -557,6 +597,11 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
           tmem_ld_wait();
           const int col = nt * 128 + c * 32;
           if (row_ok && col < p.n_out) {
+            if (p.save_gu != nullptr) {
+              __nv_bfloat16* sg = p.save_gu + (int64_t)(s_off[e] + r_local) * (2 * p.n_out) + col;
+              store_bf16x32(sg, g);
+              store_bf16x32(sg + p.n_out, u);
+            }
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -680,7 +725,8 @@ cudaError_t launch_expert_ffn_simt(const Problem& p, const void* x_packed, const
 
 cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int32_t* offsets,
                               const void* w_gate, const void* w_up, const void* w_down,
-                              void* hidden, void* y_packed, uint32_t* status, cudaStream_t s) {
+                              void* hidden, void* y_packed, uint32_t* status, cudaStream_t s,
+                              void* save_gu) {
   if (!p.bf16)
     return launch_expert_ffn_simt(p, x_packed, offsets, w_gate, w_up, w_down, hidden, y_packed, status, s);
   if (p.rows == 0) return cudaSuccess;
@@ -700,7 +746,7 @@ cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int3
     return cudaErrorInvalidValue;
   const int sms = device_sm_count();
   const int grid = pair ? (sms / 2) * 2 : sms;
-  TcParams g;
+  TcParams g = {};
   g.offsets = offsets;
   g.E = p.E;
   g.rows_cap = p.rows;
@@ -712,6 +758,7 @@ cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int3
   g.n_out = p.d_ff;
   g.out = static_cast<__nv_bfloat16*>(hidden);
   g.swap_max = swap_max_rows(g.K);
+  g.save_gu = static_cast<__nv_bfloat16*>(save_gu);
   cudaError_t e = pair ? launch_tc_pair<kEpiSwiGLU>(mA, mW1, mW3, mW1s, mW3s, g, grid, s)
                        : launch_tc<kEpiSwiGLU>(mA, mW1, mW3, g, grid, s);
   if (e != cudaSuccess) return e;
@@ -722,6 +769,7 @@ cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int3
   g.n_out = p.hu;
   g.out = static_cast<__nv_bfloat16*>(y_packed);
   g.swap_max = swap_max_rows(g.K);
+  g.save_gu = nullptr;
   return pair ? launch_tc_pair<kEpiPlain>(mH, mW2p, mW2p, mW2p, mW2p, g, grid, s)
               : launch_tc<kEpiPlain>(mH, mW2, mW2, g, grid, s);
 }

@@ -133,6 +133,38 @@ WsLayout ws_layout(const Problem& p) {
   return L;
 }
 
+// Backward scratch: the packed-row gradients and the router-gradient partials.
+struct BwdLayout {
+  size_t dy_packed;  // bf16 [T'K][h']
+  size_t dgu;        // bf16 [T'K][2·d_ff]   dG | dU
+  size_t dx_packed;  // bf16 [T'K][h']
+  size_t dgate;      // fp32 [T'][K]
+  size_t dl;         // fp32 [T'][E]
+  size_t wg_part;    // fp32 [chunks][h'][E]
+  size_t total;
+};
+
+static BwdLayout bwd_layout(const Problem& p) {
+  BwdLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += (bytes + kWsAlign - 1) / kWsAlign * kWsAlign;
+    return at;
+  };
+  const size_t rows = (size_t)p.rows, TK = (size_t)p.Tu * p.K;
+  L.dy_packed = take(rows * p.hu * 2);
+  L.dgu = take(rows * 2 * (size_t)p.d_ff * 2);
+  L.dx_packed = take(rows * p.hu * 2);
+  L.dgate = take(TK * 4);
+  L.dl = take((size_t)p.Tu * p.E * 4);
+  L.wg_part = take((size_t)backward_wg_chunks(p) * p.hu * p.E * 4);
+  L.total = off;
+  return L;
+}
+
+static bool backward_supported(const Problem& p) { return p.bf16 && p.hu % 64 == 0 && p.d_ff % 64 == 0; }
+
 }  // namespace moe
 
 using namespace moe;
@@ -248,8 +280,8 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* y_packed, const in
                                     ws_ptr<uint32_t>(ws, L.status), (cudaStream_t)stream));
 }
 
-moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
-                         const moe_outputs_t* out, void* ws, moe_stream_t stream) {
+static moe_status_t forward_impl(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
+                                 const moe_outputs_t* out, void* ws, moe_stream_t stream, void* gu) {
   Problem p;
   const moe_status_t st = make_problem(cfg, &p);
   if (st != MOE_OK) return st;
@@ -281,9 +313,82 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weigh
                       x_packed, ws, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_expert_ffn(p, x_packed, offsets_ws, w->w_gate, w->w_up, w->w_down, hidden, y_packed,
-                        status, s);
+                        status, s, gu);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_combine(p, y_packed, slot_of, gate, y, status, s);
+  return cuda_status(e);
+}
+
+moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
+                         const moe_outputs_t* out, void* ws, moe_stream_t stream) {
+  return forward_impl(cfg, x, w, y, out, ws, stream, nullptr);
+}
+
+size_t moe_saved_gu_size(const moe_config_t* cfg) {
+  Problem p;
+  if (make_problem(cfg, &p) != MOE_OK) return 0;
+  return (size_t)p.rows * 2 * (size_t)p.d_ff * 2;
+}
+
+moe_status_t moe_forward_train(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
+                               const moe_outputs_t* out, void* gu, void* ws, moe_stream_t stream) {
+  Problem p;
+  const moe_status_t st = make_problem(cfg, &p);
+  if (st != MOE_OK) return st;
+  if (!backward_supported(p)) return MOE_ERR_UNSUPPORTED;
+  if (!out || !out->topk_idx || !out->topk_gate || !out->logits || !out->slot_of) return MOE_ERR_INVALID_ARG;
+  if (p.rows > 0 && (!gu || !aligned16(gu))) return MOE_ERR_INVALID_ARG;
+  return forward_impl(cfg, x, w, y, out, ws, stream, gu);
+}
+
+size_t moe_backward_workspace_size(const moe_config_t* cfg) {
+  Problem p;
+  if (make_problem(cfg, &p) != MOE_OK || !backward_supported(p)) return 0;
+  return bwd_layout(p).total;
+}
+
+moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weights_t* w, const void* dy,
+                          float d_aux, const moe_outputs_t* out, const void* gu, void* ws,
+                          const moe_grads_t* grads, void* bws, moe_stream_t stream) {
+  Problem p;
+  const moe_status_t st = make_problem(cfg, &p);
+  if (st != MOE_OK) return st;
+  if (!backward_supported(p)) return MOE_ERR_UNSUPPORTED;
+  if (!ws_ok(ws) || !ws_ok(bws)) return MOE_ERR_WORKSPACE;
+  if (!w || !w->w_router || !w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
+  if (!out || !out->topk_idx || !out->topk_gate || !out->logits || !out->slot_of) return MOE_ERR_INVALID_ARG;
+  if (!grads || !grads->dx || !grads->dw_router || !grads->dw_gate || !grads->dw_up || !grads->dw_down)
+    return MOE_ERR_INVALID_ARG;
+  if (!isfinite(d_aux)) return MOE_ERR_INVALID_ARG;
+  if (p.Tu > 0 && (!x || !dy || !gu)) return MOE_ERR_INVALID_ARG;
+  if (!(aligned16(w->w_gate) && aligned16(w->w_up) && aligned16(w->w_down) && aligned16(grads->dw_gate) &&
+        aligned16(grads->dw_up) && aligned16(grads->dw_down) && aligned16(grads->dx) && aligned16(dy) &&
+        aligned16(gu) && aligned16(x)))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(p);
+  const BwdLayout B = bwd_layout(p);
+  const cudaStream_t s = (cudaStream_t)stream;
+  uint32_t* status = ws_ptr<uint32_t>(ws, L.status);
+  const int32_t* counts = ws_ptr<int32_t>(ws, L.counts);
+  const int32_t* offsets = ws_ptr<int32_t>(ws, L.offsets);
+  void* dy_packed = ws_ptr<void>(bws, B.dy_packed);
+  void* dgu = ws_ptr<void>(bws, B.dgu);
+  void* dx_packed = ws_ptr<void>(bws, B.dx_packed);
+  float* dgate = grads->dgate ? grads->dgate : ws_ptr<float>(bws, B.dgate);
+  float* dl = grads->dlogits ? grads->dlogits : ws_ptr<float>(bws, B.dl);
+
+  cudaError_t e = launch_backward_misc_combine(p, dy, ws_ptr<void>(ws, L.y_packed), out->slot_of, out->topk_gate,
+                                               dy_packed, dgate, status, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_backward_logits(p, out->logits, out->topk_idx, out->topk_gate, dgate, counts, d_aux, dl, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_expert_ffn_backward(p, offsets, ws_ptr<void>(ws, L.x_packed), ws_ptr<void>(ws, L.hidden), gu,
+                                 dy_packed, w->w_gate, w->w_up, w->w_down, dgu, dx_packed, grads->dw_gate,
+                                 grads->dw_up, grads->dw_down, status, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_backward_router(p, x, dl, backward_wg_chunks(p), ws_ptr<float>(bws, B.wg_part), grads->dw_router, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_backward_dx(p, dx_packed, out->slot_of, dl, ws_ptr<void>(ws, L.router_wt), grads->dx, s);
   return cuda_status(e);
 }
 

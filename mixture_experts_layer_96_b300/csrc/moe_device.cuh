@@ -166,6 +166,29 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// Descriptor of an MN-major operand written by TMA with 128-byte swizzle: boxes of 64 MN elements
+// (128 B) by K rows, one box per 64-wide MN block, `mn_block_bytes` apart. The leading-dimension
+// offset is that MN-block stride, the stride-dimension offset the 8-row K group (1024 B); a K step
+// of 16 advances the start address by 16 rows (2048 B).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t mn_block_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((mn_block_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction-descriptor bits marking A / B as MN-major (transposed) operands.
+constexpr uint32_t kIdescAMajorMN = 1u << 15;
+constexpr uint32_t kIdescBMajorMN = 1u << 16;
+
+// Make this thread's generic-proxy shared-memory writes visible to the tensor core (async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 32 TMEM lanes x 32 consecutive 32-bit columns → 32 registers per thread (lane = thread).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

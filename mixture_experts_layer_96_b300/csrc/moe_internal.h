@@ -94,9 +94,29 @@ cudaError_t launch_dispatch(const Problem& p, const void* x, const int32_t* idx,
                             int32_t* offsets, int32_t* slot_of, int32_t* row_token, void* x_packed,
                             void* ws, cudaStream_t s);
 
+// save_gu (bf16 layers): also write the SwiGLU inputs G | U as bf16 [rows][2·d_ff] for the backward.
 cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int32_t* offsets,
                               const void* w_gate, const void* w_up, const void* w_down,
-                              void* hidden, void* y_packed, uint32_t* status, cudaStream_t s);
+                              void* hidden, void* y_packed, uint32_t* status, cudaStream_t s,
+                              void* save_gu = nullptr);
+
+// ---- backward (bf16 layers, h' and d_ff multiples of 64) ---------------------------------------
+cudaError_t launch_expert_ffn_backward(const Problem& p, const int32_t* offsets, const void* x_packed,
+                                       const void* hidden, const void* gu, const void* dy_packed,
+                                       const void* w_gate, const void* w_up, const void* w_down,
+                                       void* dgu, void* dx_packed, float* dw_gate, float* dw_up,
+                                       float* dw_down, uint32_t* status, cudaStream_t s);
+cudaError_t launch_backward_misc_combine(const Problem& p, const void* dy, const void* y_packed,
+                                         const int32_t* slot_of, const float* gate, void* dy_packed,
+                                         float* dgate, uint32_t* status, cudaStream_t s);
+cudaError_t launch_backward_logits(const Problem& p, const float* logits, const int32_t* idx, const float* gate,
+                                   const float* dgate, const int32_t* counts, float d_aux, float* dl,
+                                   cudaStream_t s);
+int backward_wg_chunks(const Problem& p);
+cudaError_t launch_backward_router(const Problem& p, const void* x, const float* dl, int nchunks, float* part,
+                                   float* dw_router, cudaStream_t s);
+cudaError_t launch_backward_dx(const Problem& p, const void* dx_packed, const int32_t* slot_of, const float* dl,
+                               const void* w_router_t, void* dx, cudaStream_t s);
 
 cudaError_t launch_combine(const Problem& p, const void* y_packed, const int32_t* slot_of,
                            const float* gate, void* y, uint32_t* status, cudaStream_t s);

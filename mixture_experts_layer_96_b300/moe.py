@@ -24,7 +24,8 @@ MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_capacity", "moe_route", "moe_route_logits",
            "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_status",
-           "moe_status_string", "moe_launch_count", "moe_abi_version", "moe_dispatch_noalloc")
+           "moe_status_string", "moe_launch_count", "moe_abi_version", "moe_dispatch_noalloc",
+           "moe_saved_gu_size", "moe_forward_train", "moe_backward_workspace_size", "moe_backward")
 
 
 class MoEError(RuntimeError):
@@ -64,6 +65,12 @@ class MoEOutputs(ctypes.Structure):
                 ("offsets", ctypes.c_void_p), ("slot_of", ctypes.c_void_p), ("aux", ctypes.c_void_p)]
 
 
+class MoEGrads(ctypes.Structure):
+    _fields_ = [("dx", ctypes.c_void_p), ("dw_router", ctypes.c_void_p), ("dw_gate", ctypes.c_void_p),
+                ("dw_up", ctypes.c_void_p), ("dw_down", ctypes.c_void_p), ("dlogits", ctypes.c_void_p),
+                ("dgate", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -92,6 +99,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_launch_count": (ctypes.c_uint64, []),
         "moe_abi_version": (I32, []),
         "moe_dispatch_noalloc": (I32, [cfgp, P, P, P, P, P, P, P, P]),
+        "moe_saved_gu_size": (S, [cfgp]),
+        "moe_forward_train": (I32, [cfgp, P, ctypes.POINTER(MoEWeights), P, ctypes.POINTER(MoEOutputs), P, P, P]),
+        "moe_backward_workspace_size": (S, [cfgp]),
+        "moe_backward": (I32, [cfgp, P, ctypes.POINTER(MoEWeights), P, ctypes.c_float, ctypes.POINTER(MoEOutputs),
+                               P, P, ctypes.POINTER(MoEGrads), P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -359,6 +371,103 @@ def moe_forward(cfg: MoEConfig, x, weights: LayerWeights, *, ws: Workspace, y=No
                            ctypes.byref(co) if co is not None else None, ws.ptr, _stream(stream)),
            "moe_forward")
     return y
+
+
+# ------------------------------------------------------------------------------------------------
+# training: forward that keeps G | U, and the backward (bf16 layers, h' and d_ff multiples of 64)
+
+def saved_gu_size(cfg: MoEConfig) -> int:
+    return int(load_library().moe_saved_gu_size(ctypes.byref(cfg)))
+
+
+def moe_forward_train(cfg: MoEConfig, x, weights: LayerWeights, outputs: ForwardOutputs, *, ws: Workspace,
+                      gu=None, y=None, stream=None):
+    """moe_forward that also saves the SwiGLU inputs G | U [T'K][2·d_ff] (bf16) for moe_backward.
+    `outputs` must hold topk_idx, topk_gate, logits and slot_of. Returns (y, gu)."""
+    lib = load_library()
+    dt = cfg.torch_dtype
+    _req(x, "x", (cfg.T, cfg.h), dt)
+    weights.check(cfg)
+    rows = cfg.T_units * cfg.K
+    y = y if y is not None else torch.empty((cfg.T, cfg.h), dtype=dt, device=x.device)
+    _req(y, "y", (cfg.T, cfg.h), dt)
+    gu = gu if gu is not None else torch.empty((rows, 2 * cfg.d_ff), dtype=dt, device=x.device)
+    _req(gu, "gu", (rows, 2 * cfg.d_ff), dt)
+    cw, co = weights.c_struct(), outputs.c_struct()
+    _check(lib.moe_forward_train(ctypes.byref(cfg), _ptr(x), ctypes.byref(cw), _ptr(y), ctypes.byref(co),
+                                 _ptr(gu), ws.ptr, _stream(stream)), "moe_forward_train")
+    return y, gu
+
+
+class BackwardWorkspace:
+    """Device scratch of the backward for one config."""
+
+    def __init__(self, cfg: MoEConfig, device="cuda"):
+        self.nbytes = int(load_library().moe_backward_workspace_size(ctypes.byref(cfg)))
+        if self.nbytes == 0:
+            raise MoEError(MOE_ERR_UNSUPPORTED, "moe_backward_workspace_size")
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+
+@dataclass
+class Grads:
+    dx: torch.Tensor
+    dw_router: torch.Tensor
+    dw_gate: torch.Tensor
+    dw_up: torch.Tensor
+    dw_down: torch.Tensor
+    dlogits: Optional[torch.Tensor] = None
+    dgate: Optional[torch.Tensor] = None
+
+    @staticmethod
+    def allocate(cfg: MoEConfig, device, extras=True) -> "Grads":
+        f32, hu, E, F = torch.float32, cfg.h_unit, cfg.E, cfg.d_ff
+        return Grads(dx=torch.empty((cfg.T, cfg.h), dtype=cfg.torch_dtype, device=device),
+                     dw_router=torch.empty((hu, E), dtype=f32, device=device),
+                     dw_gate=torch.empty((E, F, hu), dtype=f32, device=device),
+                     dw_up=torch.empty((E, F, hu), dtype=f32, device=device),
+                     dw_down=torch.empty((E, hu, F), dtype=f32, device=device),
+                     dlogits=torch.empty((cfg.T_units, E), dtype=f32, device=device) if extras else None,
+                     dgate=torch.empty((cfg.T_units, cfg.K), dtype=f32, device=device) if extras else None)
+
+    def check(self, cfg: MoEConfig):
+        f32, hu, E, F = torch.float32, cfg.h_unit, cfg.E, cfg.d_ff
+        _req(self.dx, "dx", (cfg.T, cfg.h), cfg.torch_dtype)
+        _req(self.dw_router, "dw_router", (hu, E), f32)
+        _req(self.dw_gate, "dw_gate", (E, F, hu), f32)
+        _req(self.dw_up, "dw_up", (E, F, hu), f32)
+        _req(self.dw_down, "dw_down", (E, hu, F), f32)
+        if self.dlogits is not None:
+            _req(self.dlogits, "dlogits", (cfg.T_units, E), f32)
+        if self.dgate is not None:
+            _req(self.dgate, "dgate", (cfg.T_units, cfg.K), f32)
+
+    def c_struct(self) -> MoEGrads:
+        return MoEGrads(_ptr(self.dx), _ptr(self.dw_router), _ptr(self.dw_gate), _ptr(self.dw_up),
+                        _ptr(self.dw_down), _ptr(self.dlogits), _ptr(self.dgate))
+
+
+def moe_backward(cfg: MoEConfig, x, weights: LayerWeights, dy, outputs: ForwardOutputs, gu, *, ws: Workspace,
+                 bws: BackwardWorkspace, d_aux: float = 1.0, grads: Optional[Grads] = None, stream=None) -> Grads:
+    """Gradients of <dy, y> + d_aux·L_aux for the moe_forward_train that filled ws, outputs and gu
+    (routing held fixed). Returns the Grads (dW fp32, dx in x's dtype)."""
+    lib = load_library()
+    dt = cfg.torch_dtype
+    _req(x, "x", (cfg.T, cfg.h), dt)
+    _req(dy, "dy", (cfg.T, cfg.h), dt)
+    weights.check(cfg)
+    _req(gu, "gu", (cfg.T_units * cfg.K, 2 * cfg.d_ff), dt)
+    grads = grads if grads is not None else Grads.allocate(cfg, x.device)
+    grads.check(cfg)
+    cw, co, cg = weights.c_struct(), outputs.c_struct(), grads.c_struct()
+    _check(lib.moe_backward(ctypes.byref(cfg), _ptr(x), ctypes.byref(cw), _ptr(dy), ctypes.c_float(d_aux),
+                            ctypes.byref(co), _ptr(gu), ws.ptr, ctypes.byref(cg), bws.ptr, _stream(stream)),
+           "moe_backward")
+    return grads
 
 
 NOALLOC_SCRATCH_BYTES = 1 << 20

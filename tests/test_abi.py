@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol():
     lib = M.load_library()
     for n in declared_symbols():
         assert hasattr(lib, n), n
-    assert lib.moe_abi_version() == 1
+    assert lib.moe_abi_version() == 2
 
 
 def _cfg(**kw):
@@ -82,3 +82,33 @@ def test_missing_workspace_and_pointers_rejected():
 
 def test_launch_counter_is_readable_on_host():
     assert isinstance(M.launch_count(), int) and M.launch_count() >= 0
+
+
+def test_backward_sizes_and_support_on_host():
+    lib = M.load_library()
+    cfg = _cfg(T=4096, h=4096, E=8, K=2, d_ff=14336, dtype="bf16", capacity_factor=None)
+    assert M.saved_gu_size(cfg) == 8192 * 2 * 14336 * 2
+    n = lib.moe_backward_workspace_size(ctypes.byref(cfg))
+    # dY_packed, dG|dU and dX_packed dominate
+    assert n >= 8192 * (4096 + 2 * 14336 + 4096) * 2 and n % 1024 == 0
+    for bad in (_cfg(), _cfg(dtype="bf16", h=96, d_ff=128), _cfg(dtype="bf16", h=128, d_ff=96)):
+        assert lib.moe_backward_workspace_size(ctypes.byref(bad)) == 0  # fp32, or h' / d_ff not multiples of 64
+        g = M.MoEGrads()
+        assert lib.moe_backward(ctypes.byref(bad), None, None, None, ctypes.c_float(1.0), None, None, 4096,
+                                ctypes.byref(g), 4096, None) == M.MOE_ERR_UNSUPPORTED
+        assert lib.moe_forward_train(ctypes.byref(bad), None, None, None, None, None, 4096, None) \
+            == M.MOE_ERR_UNSUPPORTED
+
+
+def test_backward_rejects_missing_buffers_on_host():
+    lib = M.load_library()
+    cfg = _cfg(dtype="bf16")
+    w, o, g = M.MoEWeights(), M.MoEOutputs(), M.MoEGrads()
+    args = lambda ws, bws: (ctypes.byref(cfg), 16, ctypes.byref(w), 16, ctypes.c_float(1.0), ctypes.byref(o), 16,
+                            ws, ctypes.byref(g), bws, None)
+    assert lib.moe_backward(*args(None, 4096)) == M.MOE_ERR_WORKSPACE
+    assert lib.moe_backward(*args(4096, 4100)) == M.MOE_ERR_WORKSPACE   # misaligned backward scratch
+    assert lib.moe_backward(*args(4096, 4096)) == M.MOE_ERR_INVALID_ARG  # no weights / saved outputs
+    # the training forward needs the saved outputs
+    assert lib.moe_forward_train(ctypes.byref(cfg), 16, ctypes.byref(w), 16, None, 16, 4096, None) \
+        == M.MOE_ERR_INVALID_ARG

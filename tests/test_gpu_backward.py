@@ -1,0 +1,160 @@
+"""Parity of moe_forward_train + moe_backward against the backward oracle (GPU).
+
+The GPU's routing is first checked against the oracle (exact where the decision margin exceeds
+the logit error bound, valid elsewhere); the oracle's gradient is then taken at the GPU's picks,
+which is what the backward differentiates (routing held fixed).
+
+Tolerance, from the rounding points of the bf16 path: dY_packed, dG|dU, dX_packed, G|U and H are
+each rounded to bf16 once (unit roundoff u = 2^-8 relative per element), and every gradient is a
+sum of products of such values in fp32. A gradient element therefore carries a few u relative to
+the sum of |terms|, which for sums of mixed-sign random terms is a modest multiple of the largest
+result. The bar, per gradient tensor: max|got − ref| <= 2e-2·max|ref| and
+||got − ref||_F <= 1e-2·||ref||_F (about 2.5 u).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.moe_backward as B
+from harness import Inputs, as_f64, bits_of, check_routing, config_of, to_device, widen
+from mixture_experts_layer_96_b300 import (BackwardWorkspace, ForwardOutputs, Workspace, moe_backward,
+                                           moe_forward, moe_forward_train)
+from workloads import WORKLOADS, Generator, MoEShape, scaled
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+
+
+D_AUX = 0.7
+
+SMALL = [
+    scaled(WORKLOADS["mixtral_bf16"], T=700, h=512, d_ff=1024),
+    scaled(WORKLOADS["skewed_bf16"], T=1500, h=256, d_ff=384, E=16),                       # drops, Zipf bias
+    scaled(WORKLOADS["finegrained_bf16"], T=300, h=512, d_ff=256),                         # sigmoid, groups, K=8
+    scaled(WORKLOADS["multihead_bf16"], T=400, h=1024, d_ff=512, E=16),                    # 4 heads, h'=256
+    MoEShape("odd_tiles", T=300, h=192, E=5, K=2, d_ff=192, capacity_factor=0.9),           # partial M/N tiles
+    MoEShape("sparse_experts", T=20, h=128, E=16, K=1, d_ff=128),                           # empty experts
+    MoEShape("switch_top1", T=600, h=128, E=8, K=1, d_ff=256, capacity_factor=1.2, logit_bias="zipf1.2"),
+]
+
+
+def grad_ok(got, ref):
+    err = np.abs(got - ref)
+    scale = float(np.max(np.abs(ref))) if ref.size else 0.0
+    fro_ref = float(np.linalg.norm(ref))
+    ok_max = float(err.max(initial=0.0)) <= 2e-2 * scale + 1e-6
+    ok_fro = float(np.linalg.norm(got - ref)) <= 1e-2 * fro_ref + 1e-6
+    return ok_max and ok_fro, float(err.max(initial=0.0)), scale, float(np.linalg.norm(got - ref)) / max(fro_ref, 1e-30)
+
+
+def run_train(inp: Inputs):
+    s = inp.shape
+    cfg = config_of(s)
+    x, lw = inp.device()
+    ws = Workspace(cfg)
+    outs = ForwardOutputs.allocate(cfg, "cuda")
+    y, gu = moe_forward_train(cfg, x, lw, outs, ws=ws)
+    dy = to_device(Generator(s).dy(), True)
+    bws = BackwardWorkspace(cfg)
+    g = moe_backward(cfg, x, lw, dy, outs, gu, ws=ws, bws=bws, d_aux=D_AUX)
+    ws.check()
+    return cfg, x, lw, ws, outs, y, gu, dy, bws, g
+
+
+def gpu_picks_checked(inp: Inputs, outs):
+    s = inp.shape
+    ref = inp.oracle_forward()
+    bound = inp.logit_error_bound()
+    gidx = bits_of(outs.topk_idx).astype(np.int64)
+    key_err = bound if s.score == "softmax" else bound / 4.0
+    check_routing(gidx, ref.idx, ref.keys, key_err, s)
+    return gidx
+
+
+def oracle_grads(inp: Inputs, dy_bits, idx):
+    s = inp.shape
+    W1, W3, W2 = inp.w1, inp.w3, inp.w2
+    return B.backward(widen(inp.x, True), widen(inp.w_g, True), lambda e: (widen(W1[e], True), widen(W3[e], True),
+                      widen(W2[e], True)), widen(dy_bits, True), D_AUX, E=s.E, K=s.K, d_ff=s.d_ff, score=s.score,
+                      n_heads=s.n_heads, n_groups=s.n_groups, topk_groups=s.topk_groups,
+                      capacity_factor=s.capacity_factor, aux_alpha=s.aux_alpha, logit_bias=inp.logit_bias,
+                      select_bias=inp.select_bias, idx_override=idx)
+
+
+def check_all(inp, g, ref):
+    pairs = [("dgate", g.dgate, ref.dgate), ("dlogits", g.dlogits, ref.dlogits), ("dw_down", g.dw_down, ref.dw2),
+             ("dw_gate", g.dw_gate, ref.dw1), ("dw_up", g.dw_up, ref.dw3), ("dw_router", g.dw_router, ref.dw_g),
+             ("dx", g.dx, ref.dx)]
+    for name, got, want in pairs:
+        ok, err, scale, rel = grad_ok(as_f64(got), want)
+        assert ok, f"{name}: max err {err:.3e} vs max|ref| {scale:.3e}, relative Frobenius {rel:.3e}"
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
+def test_backward_parity_small(shape):
+    inp = Inputs.make(shape)
+    cfg, x, lw, ws, outs, y, gu, dy, bws, g = run_train(inp)
+    idx = gpu_picks_checked(inp, outs)
+    ref = oracle_grads(inp, Generator(shape).dy(), idx)
+    np.testing.assert_array_equal(bits_of(outs.slot_of), ref.slot_of)
+    check_all(inp, g, ref)
+
+
+@pytest.mark.parametrize("mode", ["single", "pair_tails_transposed", "pair_tails_plain"])
+def test_backward_parity_with_each_forward_tile_mode(mode, monkeypatch):
+    """G|U are saved by every forward epilogue: single-CTA tiles, pair tiles, transposed tails."""
+    monkeypatch.setenv("MOE_TC_PAIR", "0" if mode == "single" else "1")
+    if mode != "single":
+        monkeypatch.setenv("MOE_TC_SWAP", "1" if mode == "pair_tails_transposed" else "0")
+    shape = scaled(WORKLOADS["mixtral_bf16"], T=900, h=256, d_ff=512)
+    inp = Inputs.make(shape)
+    cfg, x, lw, ws, outs, y, gu, dy, bws, g = run_train(inp)
+    idx = gpu_picks_checked(inp, outs)
+    check_all(inp, g, oracle_grads(inp, Generator(shape).dy(), idx))
+
+
+def test_forward_train_equals_forward_and_saves_the_swiglu_inputs():
+    shape = scaled(WORKLOADS["skewed_bf16"], T=1200, h=256, d_ff=384, E=16)
+    inp = Inputs.make(shape)
+    cfg = config_of(shape)
+    x, lw = inp.device()
+    ws = Workspace(cfg)
+    y0 = moe_forward(cfg, x, lw, ws=ws)
+    outs = ForwardOutputs.allocate(cfg, "cuda")
+    y1, gu = moe_forward_train(cfg, x, lw, outs, ws=ws)
+    ws.check()
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    # G|U of each kept packed row against X_e·W1ᵀ, X_e·W3ᵀ (bf16 rounding of the fp32 result)
+    off = bits_of(outs.offsets).astype(np.int64)
+    slot = bits_of(outs.slot_of).astype(np.int64)
+    xu = widen(inp.x, True)
+    gu64 = as_f64(gu)
+    idx = bits_of(outs.topk_idx)
+    for t in range(0, shape.T_units, 37):
+        for k in range(shape.K):
+            r = slot[t, k]
+            if r < 0:
+                continue
+            e = int(idx[t, k])
+            assert off[e] <= r < off[e + 1]
+            G = widen(inp.w1[e], True) @ xu[t]
+            U = widen(inp.w3[e], True) @ xu[t]
+            want = np.concatenate([G, U])
+            assert np.max(np.abs(gu64[r] - want)) <= 2 ** -8 * np.max(np.abs(want)) + 1e-3
+
+
+def test_backward_is_deterministic():
+    shape = scaled(WORKLOADS["multihead_bf16"], T=400, h=1024, d_ff=512, E=16)
+    inp = Inputs.make(shape)
+    cfg, x, lw, ws, outs, y, gu, dy, bws, g1 = run_train(inp)
+    g2 = moe_backward(cfg, x, lw, dy, outs, gu, ws=ws, bws=bws, d_aux=D_AUX)
+    ws.check()
+    for name in ("dx", "dw_router", "dw_gate", "dw_up", "dw_down", "dlogits", "dgate"):
+        a, b = getattr(g1, name), getattr(g2, name)
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32)), name

@@ -137,6 +137,7 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
 # generator
 
 _TID_X, _TID_WG, _TID_W1, _TID_W3, _TID_W2, _TID_SB = 0, 1, 2, 3, 4, 5
+_TID_DY = 6
 _PIECE = 1 << 22  # elements per independent stream piece
 
 
@@ -256,6 +257,13 @@ class Generator:
         ranks = np.arange(1, s.E + 1, dtype=np.float64)
         w = ranks ** -1.2
         return (w / w.sum()).astype(np.float32)
+
+    def dy(self) -> np.ndarray:
+        """Upstream gradient dL/dy [T][h] ~ N(0, 1), in the layer's dtype (for backward checks)."""
+        s = self.shape
+        out = self._alloc((s.T, s.h))
+        self._fill(out, _TID_DY, 0, 1.0, self.bf16)
+        return out
 
     def logits(self, scale: float = 1.0) -> np.ndarray:
         """Seeded fp32 router logits [T'][E] ~ N(0, scale^2), for routing-stage checks."""
