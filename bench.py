@@ -279,6 +279,72 @@ def run_reference(args, shape):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------------------------ train leg
+def train_supported(shape) -> bool:
+    return shape.dtype == "bf16" and shape.h_unit % 64 == 0 and shape.d_ff % 64 == 0
+
+
+def train_leg(args, shape, cfg, x, lw, device, flush, stream):
+    """One training step of the layer = moe_forward_train + moe_backward (routing held fixed), timed
+    with CUDA events per part, inputs and the upstream gradient resident. Reported beside the
+    forward metric, not in place of it."""
+    from mixture_experts_layer_96_b300 import (BackwardWorkspace, ForwardOutputs, Grads, Workspace, launch_count,
+                                               moe_backward, moe_forward_train)
+    ws = Workspace(cfg, device=device)
+    outs = ForwardOutputs.allocate(cfg, device)
+    rows = shape.T_units * shape.K
+    gu = torch.empty((rows, 2 * shape.d_ff), dtype=x.dtype, device=device)
+    bws = BackwardWorkspace(cfg, device=device)
+    grads = Grads.allocate(cfg, device, extras=False)
+    dy_bits = Generator(shape).dy()
+    dy = torch.from_numpy(dy_bits.view(np.int16)).view(torch.bfloat16).to(device)
+    y = torch.empty_like(x)
+
+    def step():
+        moe_forward_train(cfg, x, lw, outs, ws=ws, gu=gu, y=y)
+        moe_backward(cfg, x, lw, dy, outs, gu, ws=ws, bws=bws, d_aux=1.0, grads=grads)
+
+    clk = ClockSampler(device.index or 0).start()
+    b0 = time.time()
+    n_warm = 0
+    while n_warm < max(3, args.warmup) or time.time() - b0 < min(args.min_warmup_s, 1.0):
+        step()
+        n_warm += 1
+    ws.check()
+    kept = int(outs.offsets[-1].item())
+    c0 = launch_count()
+    step()
+    per_step = launch_count() - c0
+    n = max(3, args.steps // 2)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    torch.cuda.synchronize(device)
+    t0 = time.time()
+    for i in range(n):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        moe_forward_train(cfg, x, lw, outs, ws=ws, gu=gu, y=y)
+        ev[i][1].record(stream)
+        moe_backward(cfg, x, lw, dy, outs, gu, ws=ws, bws=bws, d_aux=1.0, grads=grads)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(device)
+    t1 = time.time()
+    clk.stop()
+    ws.check()
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    bwd_flop = 12.0 * shape.h_unit * shape.d_ff * kept   # dH, dX (2x), dW2, dW1|dW3 (2x)
+    return {
+        "what": "forward_train (saves G|U) + backward (dx, dW_g, dW1, dW3, dW2; routing held fixed), d_aux=1",
+        "steps": n, "ms_per_step": fwd_ms + bwd_ms, "forward_train_ms": fwd_ms, "backward_ms": bwd_ms,
+        "tokens_per_s": shape.T / ((fwd_ms + bwd_ms) * 1e-3), "unit": "tokens/s",
+        "backward_algorithmic_flop": bwd_flop,
+        "backward_tflops_whole": bwd_flop / (bwd_ms * 1e-3) / 1e12,
+        "gpu_launches_per_step": per_step,
+        "clocks": clk.summary(t0, t1, b0, t1),
+    }
+
+
 # ------------------------------------------------------------------------------------ our arm
 def run_ours(args, shape):
     from mixture_experts_layer_96_b300 import (ForwardOutputs, Workspace, launch_count, moe_combine,
@@ -442,6 +508,10 @@ def run_ours(args, shape):
     e2e_ms = aggregate_max(e0.elapsed_time(e1) / n_e2e, world, device)
     h2d = x_host.numel() * x_host.element_size()
     d2h = y_host[0].numel() * y_host[0].element_size() + 4
+    train = None
+    if args.train and train_supported(shape):
+        del xd, yd, x_host, y_host
+        train = train_leg(args, shape, cfg, x, lw, device, flush, stream)
 
     if rank != 0:
         if world > 1:
@@ -498,6 +568,10 @@ def run_ours(args, shape):
                        "neighbouring steps overlap this step's compute on two copy streams"},
         "gpu_launches": n_launch,
     }
+    if train is not None:
+        bw_peak = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
+        train["backward_frac_of_sustained_whole"] = train["backward_tflops_whole"] / bw_peak
+        line["train"] = train
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_leg(shape, args.cpu_sample)
     print(json.dumps(line), flush=True)
@@ -519,6 +593,9 @@ def main():
     ap.add_argument("--graph", dest="graph", action="store_true", default=True,
                     help="replay the forward from a CUDA graph in the timed loop (default)")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
+    ap.add_argument("--train", dest="train", action="store_true", default=True,
+                    help="also time a training step (forward_train + backward) and report it under 'train'")
+    ap.add_argument("--no-train", dest="train", action="store_false")
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
                     help="keep warming up at least this long (steady clocks); 0 for profiling runs")
     args = ap.parse_args()
