@@ -143,3 +143,85 @@ def backward(x: np.ndarray, w_g: np.ndarray, experts: ExpertProvider, dy: np.nda
     dw_g = xu.T @ dl
     dxu = dxu + dl @ np.asarray(w_g, np.float64).T
     return Grads(merge_heads(dxu, n_heads), dw_g, dw1, dw3, dw2, dl, dgate, idx, d.slot_of)
+
+
+def backward_entries(x: np.ndarray, w_g: np.ndarray, experts: ExpertProvider, dy: np.ndarray, d_aux: float,
+                     idx: np.ndarray, *, E: int, K: int, score: str = "softmax", n_heads: int = 1,
+                     capacity_factor: Optional[float] = None, aux_alpha: float = 0.01, logit_bias=None,
+                     units=(), dw2_at=(), dw1_at=(), dw3_at=()) -> dict:
+    """Selected entries of the same gradients as `backward`, each computed from its definition,
+    for layers too large to differentiate whole.  [R14]
+
+    Routing at the picks `idx`. units: unit indices whose dgate [K], dlogits [E] and dx rows [h']
+    are returned; dw2_at (e, j, f), dw1_at / dw3_at (e, f, i): weight-gradient entries.
+    """
+    xu = split_heads(np.asarray(x, np.float64), n_heads)
+    dyu = split_heads(np.asarray(dy, np.float64), n_heads)
+    Tu, hu = xu.shape
+    idx = np.asarray(idx, np.int64)
+    l = router_logits(xu, w_g, logit_bias)
+    g = gates(l, idx, score)
+    d = dispatch(idx, E, capacity(capacity_factor, K, Tu, E))
+    dl_aux = aux_backward(l, idx, E, K, aux_alpha, score, d_aux)
+    rows_of = {}
+    for t in range(Tu):
+        for k in range(K):
+            if d.slot_of[t, k] >= 0:
+                rows_of.setdefault(int(idx[t, k]), []).append((t, k))
+    need = set(e for e, _, _ in list(dw2_at) + list(dw1_at) + list(dw3_at))
+    for u in units:
+        need.update(int(idx[u, k]) for k in range(K) if d.slot_of[u, k] >= 0)
+    out = {"dgate": {}, "dlogits": {}, "dx": {}, "dw2": {}, "dw1": {}, "dw3": {}}
+    dxp = {}  # (t, k) → dX_packed row
+    for e in sorted(need):
+        w1, w3, w2 = experts(e)
+        picks = rows_of.get(e, [])
+        if picks:
+            tok = np.array([t for t, _ in picks]); kk = np.array([k for _, k in picks])
+            X = xu[tok]
+            dY = g[tok, kk][:, None] * dyu[tok]
+        for (ee, j, f) in dw2_at:
+            if ee == e:
+                if not picks:
+                    out["dw2"][(e, j, f)] = 0.0
+                    continue
+                G, U = X @ w1[f], X @ w3[f]
+                out["dw2"][(e, j, f)] = float(np.sum(dY[:, j] * (G * sigmoid(G) * U)))
+        for key, which in (("dw1", dw1_at), ("dw3", dw3_at)):
+            for (ee, f, i) in which:
+                if ee != e:
+                    continue
+                if not picks:
+                    out[key][(e, f, i)] = 0.0
+                    continue
+                G, U = X @ w1[f], X @ w3[f]
+                sg = sigmoid(G)
+                dH = dY @ w2[:, f]
+                dcol = dH * U * sg * (1.0 + G * (1.0 - sg)) if key == "dw1" else dH * G * sg
+                out[key][(e, f, i)] = float(np.sum(dcol * X[:, i]))
+        for u in units:
+            for k in range(K):
+                if int(idx[u, k]) != e or d.slot_of[u, k] < 0:
+                    continue
+                xt = xu[u]
+                G, U = w1 @ xt, w3 @ xt
+                sg = sigmoid(G)
+                S = G * sg
+                yk = w2 @ (S * U)
+                out["dgate"][(u, k)] = float(np.dot(dyu[u], yk))
+                dYr = g[u, k] * dyu[u]
+                dH = dYr @ w2
+                dG = dH * U * sg * (1.0 + G * (1.0 - sg))
+                dU = dH * S
+                dxp[(u, k)] = dG @ w1 + dU @ w3
+    for u in units:
+        dg = np.array([out["dgate"].get((u, k), 0.0) for k in range(K)])
+        dl_u = gate_backward(l[u:u + 1], idx[u:u + 1], dg[None, :], score)[0] + dl_aux[u]
+        out["dlogits"][u] = dl_u
+        dx = dl_u @ np.asarray(w_g, np.float64).T
+        for k in range(K):
+            if (u, k) in dxp:
+                dx = dx + dxp[(u, k)]
+        out["dgate"].update({(u, k): float(dg[k]) for k in range(K)})
+        out["dx"][u] = dx
+    return out

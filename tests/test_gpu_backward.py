@@ -158,3 +158,74 @@ def test_backward_is_deterministic():
         a, b = getattr(g1, name), getattr(g2, name)
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32)), name
+
+
+# ------------------------------------------------------------------------- full-size, sampled
+FULL = ["mixtral_bf16", "skewed_bf16", "multihead_bf16", "finegrained_bf16"]
+
+
+def sampled_ok(got, want, what):
+    got, want = np.asarray(got, np.float64), np.asarray(want, np.float64)
+    scale = float(np.max(np.abs(want)))
+    err = float(np.max(np.abs(got - want)))
+    assert err <= 2e-2 * scale + 1e-6, f"{what}: max err {err:.3e} vs max|ref| {scale:.3e}"
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", FULL)
+def test_backward_parity_full_size_sampled(name):
+    """The benchmark's layers at full size, in the benchmark's launch configuration. Sampled units
+    (dgate, dlogits, whole dx rows) and sampled weight-gradient entries against the oracle's
+    entry-by-entry gradients; then a second backward with dy = 0, where dl is the aux term alone
+    and the oracle differentiates the router path whole (dW_g, dx, dlogits; expert grads exactly 0)."""
+    shape = WORKLOADS[name]
+    inp = Inputs.make(shape)
+    cfg, x, lw, ws, outs, y, gu, dy, bws, g = run_train(inp)
+    ref = inp.oracle_forward(sample_units=np.array([0]))   # routing of all units; y of one
+    bound = inp.logit_error_bound()
+    gidx = bits_of(outs.topk_idx).astype(np.int64)
+    key_err = bound if shape.score == "softmax" else bound / 4.0
+    check_routing(gidx, ref.idx, ref.keys, key_err, shape)
+    counts = np.bincount(gidx.reshape(-1), minlength=shape.E)
+    slot = bits_of(outs.slot_of)
+    rng = np.random.default_rng(321)
+    units = np.sort(rng.choice(shape.T_units, size=6, replace=False))
+    live = [e for e in range(shape.E) if counts[e] > 0 and np.any(gidx[slot >= 0] == e)]
+    def at(n, d0, d1):
+        return [(int(rng.choice(live)), int(rng.integers(d0)), int(rng.integers(d1))) for _ in range(n)]
+    hu, F = shape.h_unit, shape.d_ff
+    at2, at1, at3 = at(10, hu, F), at(10, F, hu), at(10, F, hu)
+    W1, W3, W2 = inp.w1, inp.w3, inp.w2
+    ex = lambda e: (widen(W1[e], True), widen(W3[e], True), widen(W2[e], True))
+    dy_bits = Generator(shape).dy()
+    ent = B.backward_entries(widen(inp.x, True), widen(inp.w_g, True), ex, widen(dy_bits, True), D_AUX, gidx,
+                             E=shape.E, K=shape.K, score=shape.score, n_heads=shape.n_heads,
+                             capacity_factor=shape.capacity_factor, aux_alpha=shape.aux_alpha,
+                             logit_bias=inp.logit_bias, units=units, dw2_at=at2, dw1_at=at1, dw3_at=at3)
+    H = shape.n_heads
+    dx_units = g.dx.view(shape.T_units, hu)
+    sampled_ok([float(g.dgate[u, k]) for u in units for k in range(shape.K)],
+               [ent["dgate"][(u, k)] for u in units for k in range(shape.K)], "dgate")
+    sampled_ok(np.stack([as_f64(g.dlogits[u]) for u in units]), np.stack([ent["dlogits"][u] for u in units]), "dlogits")
+    for u in units:
+        sampled_ok(as_f64(dx_units[u]), ent["dx"][u], f"dx[{u}]")
+    for key, ats, t in (("dw2", at2, g.dw_down), ("dw1", at1, g.dw_gate), ("dw3", at3, g.dw_up)):
+        sampled_ok([float(t[a]) for a in ats], [ent[key][a] for a in ats], key)
+
+    # dy = 0: dl = d_aux·(aux gradient) for every unit; the router path is checked whole
+    zero = torch.zeros_like(dy)
+    g0 = moe_backward(cfg, x, lw, zero, outs, gu, ws=ws, bws=bws, d_aux=1.0, grads=g)  # reuses g's buffers
+    ws.check()
+    l = ref.logits
+    dl = B.aux_backward(l, gidx, shape.E, shape.K, shape.aux_alpha, shape.score, 1.0)
+    xu = O_split(widen(inp.x, True), H)
+    sampled_ok(as_f64(g0.dlogits), dl, "dlogits (aux only)")
+    sampled_ok(as_f64(g0.dw_router), xu.T @ dl, "dW_g (aux only)")
+    sampled_ok(as_f64(g0.dx.view(shape.T_units, hu)), dl @ widen(inp.w_g, True).T, "dx (aux only)")
+    for name_, t in (("dw_down", g0.dw_down), ("dw_gate", g0.dw_gate), ("dw_up", g0.dw_up)):
+        assert int(torch.count_nonzero(t)) == 0, name_
+
+
+def O_split(x, H):
+    import oracle.moe_oracle as O
+    return O.split_heads(x, H)

@@ -173,3 +173,25 @@ def test_pin_catches_an_aux_gradient_with_the_wrong_sign(monkeypatch):
     right = B.aux_backward
     assert fd_check_fails(monkeypatch, "aux_backward", lambda *a: -right(*a),
                           dict(E=6, K=2, score="sigmoid", aux_alpha=0.5))
+
+
+@pytest.mark.parametrize("cfg", CONFIGS[:4], ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_entry_oracle_equals_the_whole_gradient(cfg):
+    """backward_entries (used where the layer is too large to differentiate whole) gives the same
+    numbers as backward, entry by entry."""
+    p, kw = case_for(cfg)
+    ex = lambda e: (p["w1"][e], p["w3"][e], p["w2"][e])
+    g = grads_of(p, kw)
+    keep = {k: v for k, v in kw.items() if k in ("E", "K", "score", "n_heads", "capacity_factor", "aux_alpha")}
+    units = [0, 5, 11]
+    at2, at1, at3 = [(1, 2, 3), (5, 7, 9)], [(0, 4, 6), (3, 9, 1)], [(2, 0, 7), (4, 8, 2)]
+    r = B.backward_entries(p["x"], p["w_g"], ex, p["dy"], kw_d_aux(kw), g.idx, logit_bias=p["logit_bias"],
+                           units=units, dw2_at=at2, dw1_at=at1, dw3_at=at3, **keep)
+    for u in units:
+        np.testing.assert_allclose(r["dlogits"][u], g.dlogits[u], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(r["dx"][u], O.split_heads(g.dx, kw.get("n_heads", 1))[u], rtol=1e-12, atol=1e-14)
+        for k in range(cfg["K"]):
+            assert r["dgate"][(u, k)] == pytest.approx(g.dgate[u, k], rel=1e-12, abs=1e-14)
+    for key, at, full in (("dw2", at2, g.dw2), ("dw1", at1, g.dw1), ("dw3", at3, g.dw3)):
+        for a in at:
+            assert r[key][a] == pytest.approx(full[a], rel=1e-12, abs=1e-14)
