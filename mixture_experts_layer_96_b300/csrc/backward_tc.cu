@@ -57,12 +57,6 @@ struct BwdParams {
   uint32_t* status;
 };
 
-__device__ __forceinline__ void store_f32x32(float* dst, const uint32_t (&v)[32]) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) d4[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
@@ -71,6 +65,8 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_pre[kMaxExperts + 1];
   __shared__ __align__(8) uint64_t s_bar[2 * kStages + 5];
+  // DW epilogue: per epilogue warp a 32 x 32 fp32 chunk, 16-byte pieces XOR-swizzled by row
+  __shared__ __align__(16) float s_epi[MODE == kModeDW ? 4 * 32 * 32 : 4];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_ok;
@@ -145,20 +141,19 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
           const uint32_t sa = sbase + stage * kStageBytes, sb = sa + kABytes;
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, kStageBytes);
+          // MN-major operands come through 3-D maps: one request per operand for all of its
+          // 64-column blocks (A: 2, B: 4), each landing as an 8 KB swizzled tile
           if (MODE == kModeDW) {
             const int r0 = s_off[e] + kb * kBK;  // K rows of this block (the expert's packed rows)
-#pragma unroll
-            for (int a = 0; a < kBM / 64; ++a) tma_load_2d(sa + a * kMnBox, &tmA, fb, mt * kBM + a * 64, r0);
-#pragma unroll
-            for (int b = 0; b < kBN / 64; ++b) tma_load_2d(sb + b * kMnBox, &tmB0, fb, nt * kBN + b * 64, r0);
+            tma_load_3d(sa, &tmA, fb, 0, r0, mt * (kBM / 64));
+            tma_load_3d(sb, &tmB0, fb, 0, r0, nt * (kBN / 64));
           } else {
             tma_load_2d(sa, &tmA, fb, kb * kBK, s_off[e] + mt * kBM);
             const int kk = kb * kBK;
             const bool second = MODE == kModeDX && kk >= p.k_split;
             const CUtensorMap* mb = second ? &tmB1 : &tmB0;
             const int brow = e * p.w_rows + (second ? kk - p.k_split : kk);
-#pragma unroll
-            for (int b = 0; b < kBN / 64; ++b) tma_load_2d(sb + b * kMnBox, mb, fb, nt * kBN + b * 64, brow);
+            tma_load_3d(sb, mb, fb, 0, brow, nt * (kBN / 64));
           }
           filled |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -248,14 +243,15 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       tc_fence_after();
       const uint32_t t_row = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(q * 32) << 16);
       if (MODE == kModeDW) {
-        const int m = mt * kBM + q * 32 + lane;
-        float* orow = nullptr;
-        if (m < p.m_total) {
-          orow = m < p.m_split ? p.out_a + ((int64_t)e * p.m_split + m) * p.n_out
-                               : p.out_b + ((int64_t)e * (p.m_total - p.m_split) + (m - p.m_split)) * p.n_out;
-        }
+        // A lane holds one output row of the chunk. Staged in shared memory, the chunk goes out
+        // row-contiguously: per store instruction 8 lanes cover one 128-byte row piece, so a warp
+        // writes 4 whole lines instead of 32 scattered 16-byte fragments.
+        float* stg = s_epi + (warp - 2) * 32 * 32;
+        const int sub = lane >> 3, piece = lane & 7;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
+          const int col = nt * kBN + c * 32;
+          if (col >= p.n_out) break;  // n_out is a multiple of 64: chunks past it are whole
           uint32_t v[32];
           if (nkb > 0) {
             tmem_ld_32x32b_x32(t_row + c * 32, v);
@@ -264,8 +260,24 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = 0u;
           }
-          const int col = nt * kBN + c * 32;
-          if (orow != nullptr && col < p.n_out) store_f32x32(orow + col, v);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(stg + lane * 32 + ((j ^ (lane & 7)) * 4)) =
+                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = i * 4 + sub;
+            const int m = mt * kBM + q * 32 + r;
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 32 + ((piece ^ (r & 7)) * 4));
+            if (m < p.m_total) {
+              float* orow = m < p.m_split
+                                ? p.out_a + ((int64_t)e * p.m_split + m) * p.n_out
+                                : p.out_b + ((int64_t)e * (p.m_total - p.m_split) + (m - p.m_split)) * p.n_out;
+              *reinterpret_cast<uint4*>(orow + col + piece * 4) = val;
+            }
+          }
+          __syncwarp();
         }
       } else {
         const int rows_e = s_off[e + 1] - s_off[e];
@@ -377,15 +389,16 @@ cudaError_t launch_expert_ffn_backward(const Problem& p, const int32_t* offsets,
   const uint64_t rows = (uint64_t)(p.rows > 0 ? p.rows : 1);
   const uint64_t E = (uint64_t)p.E, hu = (uint64_t)p.hu, dff = (uint64_t)p.d_ff;
   CUtensorMap mDYk, mDGUk, mW2, mW1, mW3, mDYm, mH, mDGUm, mX;
+  const uint32_t nbA = kBM / 64, nbB = kBN / 64;  // 64-column blocks per MN-major A / B box
   if (!encode_tmap_2d_bf16(&mDYk, dy_packed, hu, rows, kBK, kBM) ||
       !encode_tmap_2d_bf16(&mDGUk, dgu, 2 * dff, rows, kBK, kBM) ||
-      !encode_tmap_2d_bf16(&mW2, w_down, dff, E * hu, 64, kBK) ||
-      !encode_tmap_2d_bf16(&mW1, w_gate, hu, E * dff, 64, kBK) ||
-      !encode_tmap_2d_bf16(&mW3, w_up, hu, E * dff, 64, kBK) ||
-      !encode_tmap_2d_bf16(&mDYm, dy_packed, hu, rows, 64, kBK) ||
-      !encode_tmap_2d_bf16(&mH, hidden, dff, rows, 64, kBK) ||
-      !encode_tmap_2d_bf16(&mDGUm, dgu, 2 * dff, rows, 64, kBK) ||
-      !encode_tmap_2d_bf16(&mX, x_packed, hu, rows, 64, kBK))
+      !encode_tmap_mn_blocks_bf16(&mW2, w_down, dff, E * hu, kBK, nbB) ||
+      !encode_tmap_mn_blocks_bf16(&mW1, w_gate, hu, E * dff, kBK, nbB) ||
+      !encode_tmap_mn_blocks_bf16(&mW3, w_up, hu, E * dff, kBK, nbB) ||
+      !encode_tmap_mn_blocks_bf16(&mDYm, dy_packed, hu, rows, kBK, nbA) ||
+      !encode_tmap_mn_blocks_bf16(&mH, hidden, dff, rows, kBK, nbB) ||
+      !encode_tmap_mn_blocks_bf16(&mDGUm, dgu, 2 * dff, rows, kBK, nbA) ||
+      !encode_tmap_mn_blocks_bf16(&mX, x_packed, hu, rows, kBK, nbB))
     return cudaErrorInvalidValue;
   const int64_t m_tiles_rows = (p.rows + kBM - 1) / kBM + p.E;  // upper bound of the M-grouped m-tiles
 

@@ -58,6 +58,19 @@ bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tmap_mn_blocks_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                                uint32_t box_rows, uint32_t blocks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || (reinterpret_cast<uintptr_t>(base) & 15) != 0 || cols % 64 != 0) return false;
+  const cuuint64_t dims[3] = {64, rows, cols / 64};
+  const cuuint64_t strides[2] = {cols * 2, 128};
+  const cuuint32_t box[3] = {64, box_rows, blocks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 moe_status_t make_problem(const moe_config_t* c, Problem* p) {
   if (!c || !p) return MOE_ERR_INVALID_ARG;
   if (c->T < 0 || c->h < 1 || c->n_heads < 1 || c->h % c->n_heads != 0) return MOE_ERR_INVALID_ARG;

@@ -81,6 +81,12 @@ void note_launch(int n = 1);
 bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                          uint32_t box_inner, uint32_t box_outer);
 
+// A row-major bf16 matrix [rows][cols] (cols a multiple of 64) as the 3-D tensor
+// {64 elements, rows, cols/64 column blocks}: a box of `box_rows` rows by `blocks` column blocks
+// lands in shared memory as `blocks` MN-major 128-byte-swizzled tiles, box_rows·128 bytes apart.
+bool encode_tmap_mn_blocks_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                                uint32_t box_rows, uint32_t blocks);
+
 // ---- launchers (return cudaSuccess or the launch error) --------------------------------------
 cudaError_t launch_route(const Problem& p, const void* x, const void* w_router,
                          const float* logits_in, const float* logit_bias, const float* select_bias,
