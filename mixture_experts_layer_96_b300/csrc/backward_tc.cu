@@ -12,10 +12,13 @@
 //           A (dY or dG|dU) is K-major; B (W2, or W1 then W3) is read in its stored layout,
 //           which is MN-major for these products (the descriptors say so; no transposed copies).
 //   DW      K-grouped: for every expert a dense [M][N] tile grid, the reduction running over the
-//           expert's rows. Both operands are packed activations, MN-major. The last k-block of
-//           an expert usually extends into the next expert's rows: the MMA warp's 32 lanes zero
-//           those K rows in shared memory before the MMA (then a proxy fence), so they add
-//           nothing. An expert without rows gets a zero tile.
+//           expert's rows. A comes K-major from a transposed copy of packed rows in which every
+//           expert's rows start at a multiple of 64 and are zero-padded to one (an MN-major A ran
+//           at about half the tensor rate); B is packed rows read MN-major. B's last k-block
+//           usually extends into the next expert's rows: the MMA warp's 32 lanes zero those K rows
+//           in shared memory before the MMA (then a proxy fence), so no non-finite leftover can
+//           meet A's zero padding. An expert without rows gets a zero tile. dW1|dW3 come out
+//           transposed (M = h', N = 2·d_ff) and are stored row by row of the weight.
 //   warp 0     TMA producer (one lane)
 //   warp 1     TMEM allocator + MMA issuer (lane 0 issues; all lanes zero K tails in DW)
 //   warps 2-5  epilogue: tcgen05.ld → SwiGLU backward / bf16 / fp32 stores
@@ -49,10 +52,11 @@ struct BwdParams {
   int n_tiles;                   // ceil(n_out / 256)
   int m_tiles;                   // DW: ceil(m_total / 128)
   int m_total;                   // DW: M extent (h' for dW2, 2·d_ff for dW1|dW3)
-  int m_split;                   // DW: rows m >= m_split go to out_b (dW3), else out_a
+  int n_split;                   // DW transposed output: columns n >= n_split go to out_b (dW3)
+  int transposed_out;            // DW: 0 → out_a[e][m][n]; 1 → out_{a|b}[e][n][m] (dW1|dW3)
   __nv_bfloat16* out_bf16;       // DH: dG|dU [rows][2·d_ff]; DX: dX_packed [rows][h']
   const __nv_bfloat16* gu;       // DH: G|U [rows][2·d_ff]
-  float* out_a;                  // DW: dW2 [E][h'][d_ff], or dW1 [E][d_ff][h']
+  float* out_a;                  // DW: dW2 [E][h'][d_ff], or dW1 [E][d_ff][h'] (transposed output)
   float* out_b;                  // DW: dW3 [E][d_ff][h'] (null for dW2)
   uint32_t* status;
 };
@@ -60,13 +64,15 @@ struct BwdParams {
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                     const __grid_constant__ CUtensorMap tmB1, BwdParams p) {
+                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
+                     const __grid_constant__ CUtensorMap tmO1, BwdParams p) {
   extern __shared__ unsigned char smem_dyn[];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_pre[kMaxExperts + 1];
   __shared__ __align__(8) uint64_t s_bar[2 * kStages + 5];
   // DW epilogue: per epilogue warp a 32 x 32 fp32 chunk, 16-byte pieces XOR-swizzled by row
-  __shared__ __align__(16) float s_epi[MODE == kModeDW ? 4 * 32 * 32 : 4];
+  // DW: per epilogue warp a 32 x 32 fp32 tile in the 128-byte-swizzle layout of the store's map
+  __shared__ __align__(1024) float s_epi[MODE == kModeDW ? 4 * 32 * 32 : 4];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_ok;
@@ -81,7 +87,8 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
   const uint32_t done_bar = bar0 + 8u * (2 * kStages + 4);
 
   if (warp == 0) {
-    const bool ok = warp_tile_prefix(p.offsets, p.E, kBM, p.rows_cap, s_off, s_pre);
+    // M-grouped: m-tile prefix (128 rows); DW: 64-row block prefix = A's padded column offsets / 64
+    const bool ok = warp_tile_prefix(p.offsets, p.E, MODE == kModeDW ? kBK : kBM, p.rows_cap, s_off, s_pre);
     if (lane == 0) {
       s_ok = ok ? 1 : 0;
       s_abort = 0;
@@ -99,6 +106,10 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB0);
       if (MODE == kModeDX) tma_prefetch_desc(&tmB1);
+      if (MODE == kModeDW) {
+        tma_prefetch_desc(&tmO0);
+        tma_prefetch_desc(&tmO1);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -115,11 +126,13 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
   // (expert, m-tile, n-tile) of a linear tile index, and the k-blocks it runs
   auto tile_coords = [&](int tile, int& e, int& mt, int& nt, int& nkb) {
     if (MODE == kModeDW) {
+      // m-tiles fastest: the tiles in flight share B's n-block (read from DRAM once) and cycle
+      // through the expert's small transposed A (it stays in L2 while the fp32 output streams out)
       const int per_e = p.m_tiles * p.n_tiles;
       e = tile / per_e;
       const int r = tile - e * per_e;
-      mt = r / p.n_tiles;
-      nt = r - mt * p.n_tiles;
+      nt = r / p.m_tiles;
+      mt = r - nt * p.m_tiles;
       nkb = (s_off[e + 1] - s_off[e] + kBK - 1) / kBK;
     } else {
       decode_tile(tile, s_pre, p.E, p.n_tiles, e, mt, nt);
@@ -144,9 +157,10 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
           // MN-major operands come through 3-D maps: one request per operand for all of its
           // 64-column blocks (A: 2, B: 4), each landing as an 8 KB swizzled tile
           if (MODE == kModeDW) {
-            const int r0 = s_off[e] + kb * kBK;  // K rows of this block (the expert's packed rows)
-            tma_load_3d(sa, &tmA, fb, 0, r0, mt * (kBM / 64));
-            tma_load_3d(sb, &tmB0, fb, 0, r0, nt * (kBN / 64));
+            // A: K-major from the padded transposed copy (columns 64·s_pre[e] + ...); B: the same K
+            // rows of the packed activations, MN-major
+            tma_load_2d(sa, &tmA, fb, (s_pre[e] + kb) * kBK, mt * kBM);
+            tma_load_3d(sb, &tmB0, fb, 0, s_off[e] + kb * kBK, nt * (kBN / 64));
           } else {
             tma_load_2d(sa, &tmA, fb, kb * kBK, s_off[e] + mt * kBM);
             const int kk = kb * kBK;
@@ -170,8 +184,7 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (lane 0) + K-tail zeroing
-    constexpr uint32_t idesc =
-        idesc_bf16_f32(kBM, kBN) | kIdescBMajorMN | (MODE == kModeDW ? kIdescAMajorMN : 0u);
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN) | kIdescBMajorMN;
     int stage = 0;
     uint32_t phase = 0;
     bool aborted = false;
@@ -190,13 +203,13 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         if (MODE == kModeDW) {
           const int valid = s_off[e + 1] - s_off[e] - kb * kBK;
           if (valid < kBK) {
-            // zero K rows valid..63 of the 2 A boxes and the 4 B boxes (one 128-byte row each)
-            const int nrow = (kBK - valid) * (kBM / 64 + kBN / 64);
+            // zero K rows valid..63 of the 4 B boxes (one 128-byte row each)
+            const int nrow = (kBK - valid) * (kBN / 64);
             for (int i = lane; i < nrow * 8; i += 32) {
               const int row = i >> 3, chunk = i & 7;
               const int box = row / (kBK - valid), r = valid + row % (kBK - valid);
-              const uint32_t base = box < kBM / 64 ? sa + box * kMnBox : sb + (box - kBM / 64) * kMnBox;
-              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(base + r * 128 + chunk * 16), "r"(0u)
+              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sb + box * kMnBox + r * 128 + chunk * 16),
+                           "r"(0u)
                            : "memory");
             }
             fence_proxy_async_smem();
@@ -208,7 +221,7 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
           uint64_t ad, bd;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            ad = MODE == kModeDW ? sdesc_mnmajor_sw128(sa + k * 2048, kMnBox) : sdesc_kmajor_sw128(sa) + (uint64_t)(2 * k);
+            ad = sdesc_kmajor_sw128(sa) + (uint64_t)(2 * k);
             bd = sdesc_mnmajor_sw128(sb + k * 2048, kMnBox);
             umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
@@ -243,11 +256,13 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       tc_fence_after();
       const uint32_t t_row = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(q * 32) << 16);
       if (MODE == kModeDW) {
-        // A lane holds one output row of the chunk. Staged in shared memory, the chunk goes out
-        // row-contiguously: per store instruction 8 lanes cover one 128-byte row piece, so a warp
-        // writes 4 whole lines instead of 32 scattered 16-byte fragments.
+        // A lane holds row m of the chunk's 32 x 32 fp32 block. It is staged in shared memory in
+        // the 128-byte-swizzle layout (16-byte piece j of row r at piece j ^ (r & 7)) and one lane
+        // writes it out with a TMA store: rows m of dW2[e], or, transposed, rows n of dW1 / dW3[e]
+        // (the block staged with n as its row). Rows and columns past the tensor are not written.
         float* stg = s_epi + (warp - 2) * 32 * 32;
-        const int sub = lane >> 3, piece = lane & 7;
+        const uint32_t stg_addr = smem_addr(stg);
+        const int m0 = mt * kBM + q * 32;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           const int col = nt * kBN + c * 32;
@@ -260,24 +275,26 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = 0u;
           }
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(stg + lane * 32 + ((j ^ (lane & 7)) * 4)) =
-                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          if (lane == 0) bulk_wait_group_read0();  // the previous store has read the tile
           __syncwarp();
+          if (!p.transposed_out) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = i * 4 + sub;
-            const int m = mt * kBM + q * 32 + r;
-            const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 32 + ((piece ^ (r & 7)) * 4));
-            if (m < p.m_total) {
-              float* orow = m < p.m_split
-                                ? p.out_a + ((int64_t)e * p.m_split + m) * p.n_out
-                                : p.out_b + ((int64_t)e * (p.m_total - p.m_split) + (m - p.m_split)) * p.n_out;
-              *reinterpret_cast<uint4*>(orow + col + piece * 4) = val;
-            }
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(stg + lane * 32 + ((j ^ (lane & 7)) * 4)) =
+                  make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)  // row n = j, column m = lane
+              stg[j * 32 + ((((lane >> 2) ^ (j & 7)) << 2) | (lane & 3))] = __uint_as_float(v[j]);
           }
+          fence_proxy_async_smem();
           __syncwarp();
+          if (lane == 0) {
+            if (!p.transposed_out) tma_store_3d(&tmO0, stg_addr, col, m0, e);
+            else if (col < p.n_split) tma_store_3d(&tmO0, stg_addr, m0, col, e);
+            else tma_store_3d(&tmO1, stg_addr, m0, col - p.n_split, e);
+            bulk_commit_group();
+          }
         }
       } else {
         const int rows_e = s_off[e + 1] - s_off[e];
@@ -349,6 +366,8 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
     }
+    if (MODE == kModeDW && lane == 0) bulk_wait_group0();  // every output tile written
+    __syncwarp();
   }
 
   __syncthreads();
@@ -359,8 +378,8 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
 }
 
 template <int MODE>
-cudaError_t launch_bwd(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const BwdParams& p,
-                       int64_t max_tiles, cudaStream_t s) {
+cudaError_t launch_bwd(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& o0,
+                       const CUtensorMap& o1, const BwdParams& p, int64_t max_tiles, cudaStream_t s) {
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -372,12 +391,68 @@ cudaError_t launch_bwd(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
   }
   const int sms = device_sm_count();
   const int grid = (int)(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
-  expert_bwd_tc_kernel<MODE><<<grid, kThreads, kSmem, s>>>(a, b0, b1, p);
+  expert_bwd_tc_kernel<MODE><<<grid, kThreads, kSmem, s>>>(a, b0, b1, o0, o1, p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// Packed rows [rows][cols] (bf16; expert e's rows are offsets[e]..offsets[e+1]) → transposed
+// [cols][pcols]: expert e's rows become columns 64·P_e .. 64·P_e + 64·ceil(n_e/64), with
+// P_e = Σ_{e'<e} ceil(n_e'/64), zero past its n_e rows. One block per 64 x 64 tile.
+__global__ void __launch_bounds__(256) transpose_pad_kernel(const __nv_bfloat16* __restrict__ in,
+                                                            const int32_t* __restrict__ offsets, int E,
+                                                            int64_t rows_cap, int cols, int64_t pcols,
+                                                            __nv_bfloat16* __restrict__ out) {
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_pre[kMaxExperts + 1];
+  __shared__ __align__(16) uint16_t tile[64][64 + 8];  // [row k][column i]
+  __shared__ int s_ok;
+  if (threadIdx.x < 32) {
+    const bool ok = warp_tile_prefix(offsets, E, 64, rows_cap, s_off, s_pre);
+    if (threadIdx.x == 0) s_ok = ok ? 1 : 0;
+  }
+  __syncthreads();
+  const int cb = blockIdx.y;
+  if (!s_ok || cb >= s_pre[E]) return;
+  int lo = 0, hi = E - 1;  // the expert whose blocks contain cb (largest e with s_pre[e] <= cb)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_pre[mid] <= cb) lo = mid;
+    else hi = mid - 1;
+  }
+  const int r0 = s_off[lo] + (cb - s_pre[lo]) * 64;
+  const int valid = min(64, s_off[lo + 1] - r0);
+  const int i0 = blockIdx.x * 64;
+  for (int j = threadIdx.x; j < 64 * 8; j += 256) {
+    const int k = j >> 3, v = j & 7;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (k < valid && i0 + v * 8 < cols) val = *reinterpret_cast<const uint4*>(in + (int64_t)(r0 + k) * cols + i0 + v * 8);
+    *reinterpret_cast<uint4*>(&tile[k][v * 8]) = val;
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < 64 * 8; j += 256) {
+    const int i = j >> 3, v = j & 7;
+    if (i0 + i >= cols) continue;
+    uint32_t w[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) w[t] = (uint32_t)tile[v * 8 + 2 * t][i] | ((uint32_t)tile[v * 8 + 2 * t + 1][i] << 16);
+    *reinterpret_cast<uint4*>(out + (int64_t)(i0 + i) * pcols + (int64_t)cb * 64 + v * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+cudaError_t launch_transpose_pad(const Problem& p, const void* in, const int32_t* offsets, int cols, int64_t pcols,
+                                 void* out, cudaStream_t s) {
+  const dim3 grid((unsigned)((cols + 63) / 64), (unsigned)(pcols / 64));
+  transpose_pad_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in), offsets, p.E, p.rows, cols, pcols,
+                                            static_cast<__nv_bfloat16*>(out));
   note_launch();
   return cudaGetLastError();
 }
 
 }  // namespace
+
+// Columns of the padded transposed copies: every expert's rows rounded up to 64.
+int64_t backward_padded_cols(const Problem& p) { return 64 * ((p.rows + 63) / 64 + p.E); }
 
 // dY_packed, saved G|U, X_packed, H → dG|dU, dX_packed, dW1, dW3, dW2 (bf16 layers; h' and d_ff
 // multiples of 64, checked by the caller).
@@ -385,20 +460,21 @@ cudaError_t launch_expert_ffn_backward(const Problem& p, const int32_t* offsets,
                                        const void* hidden, const void* gu, const void* dy_packed,
                                        const void* w_gate, const void* w_up, const void* w_down,
                                        void* dgu, void* dx_packed, float* dw_gate, float* dw_up,
-                                       float* dw_down, uint32_t* status, cudaStream_t s) {
+                                       float* dw_down, void* dy_t, void* x_t, uint32_t* status, cudaStream_t s) {
   const uint64_t rows = (uint64_t)(p.rows > 0 ? p.rows : 1);
   const uint64_t E = (uint64_t)p.E, hu = (uint64_t)p.hu, dff = (uint64_t)p.d_ff;
-  CUtensorMap mDYk, mDGUk, mW2, mW1, mW3, mDYm, mH, mDGUm, mX;
-  const uint32_t nbA = kBM / 64, nbB = kBN / 64;  // 64-column blocks per MN-major A / B box
+  const int64_t pcols = backward_padded_cols(p);
+  CUtensorMap mDYk, mDGUk, mW2, mW1, mW3, mDYt, mH, mDGUm, mXt;
+  const uint32_t nbB = kBN / 64;  // 64-column blocks per MN-major B box
   if (!encode_tmap_2d_bf16(&mDYk, dy_packed, hu, rows, kBK, kBM) ||
       !encode_tmap_2d_bf16(&mDGUk, dgu, 2 * dff, rows, kBK, kBM) ||
       !encode_tmap_mn_blocks_bf16(&mW2, w_down, dff, E * hu, kBK, nbB) ||
       !encode_tmap_mn_blocks_bf16(&mW1, w_gate, hu, E * dff, kBK, nbB) ||
       !encode_tmap_mn_blocks_bf16(&mW3, w_up, hu, E * dff, kBK, nbB) ||
-      !encode_tmap_mn_blocks_bf16(&mDYm, dy_packed, hu, rows, kBK, nbA) ||
+      !encode_tmap_2d_bf16(&mDYt, dy_t, (uint64_t)pcols, hu, kBK, kBM) ||
       !encode_tmap_mn_blocks_bf16(&mH, hidden, dff, rows, kBK, nbB) ||
-      !encode_tmap_mn_blocks_bf16(&mDGUm, dgu, 2 * dff, rows, kBK, nbA) ||
-      !encode_tmap_mn_blocks_bf16(&mX, x_packed, hu, rows, kBK, nbB))
+      !encode_tmap_mn_blocks_bf16(&mDGUm, dgu, 2 * dff, rows, kBK, nbB) ||
+      !encode_tmap_2d_bf16(&mXt, x_t, (uint64_t)pcols, hu, kBK, kBM))
     return cudaErrorInvalidValue;
   const int64_t m_tiles_rows = (p.rows + kBM - 1) / kBM + p.E;  // upper bound of the M-grouped m-tiles
 
@@ -415,7 +491,7 @@ cudaError_t launch_expert_ffn_backward(const Problem& p, const int32_t* offsets,
   b.n_tiles = (p.d_ff + kBN - 1) / kBN;
   b.out_bf16 = static_cast<__nv_bfloat16*>(dgu);
   b.gu = static_cast<const __nv_bfloat16*>(gu);
-  cudaError_t e = launch_bwd<kModeDH>(mDYk, mW2, mW2, b, m_tiles_rows * b.n_tiles, s);
+  cudaError_t e = launch_bwd<kModeDH>(mDYk, mW2, mW2, mW2, mW2, b, m_tiles_rows * b.n_tiles, s);
   if (e != cudaSuccess) return e;
 
   // DX: dX = dG·W1 + dU·W3
@@ -426,30 +502,41 @@ cudaError_t launch_expert_ffn_backward(const Problem& p, const int32_t* offsets,
   b.n_tiles = (p.hu + kBN - 1) / kBN;
   b.out_bf16 = static_cast<__nv_bfloat16*>(dx_packed);
   b.gu = nullptr;
-  e = launch_bwd<kModeDX>(mDGUk, mW1, mW3, b, m_tiles_rows * b.n_tiles, s);
+  e = launch_bwd<kModeDX>(mDGUk, mW1, mW3, mW1, mW1, b, m_tiles_rows * b.n_tiles, s);
   if (e != cudaSuccess) return e;
 
-  // DW: dW2 = dYᵀ·H  ([E][h'][d_ff])
+  // DW: dW2 = dYᵀ·H ([E][h'][d_ff]): A = dY transposed (K-major), B = H (MN-major)
+  e = launch_transpose_pad(p, dy_packed, offsets, p.hu, pcols, dy_t, s);
+  if (e != cudaSuccess) return e;
   b.out_bf16 = nullptr;
   b.m_total = p.hu;
-  b.m_split = p.hu;
   b.m_tiles = (p.hu + kBM - 1) / kBM;
   b.n_out = p.d_ff;
   b.n_tiles = (p.d_ff + kBN - 1) / kBN;
+  b.transposed_out = 0;
   b.out_a = dw_down;
   b.out_b = nullptr;
-  e = launch_bwd<kModeDW>(mDYm, mH, mH, b, (int64_t)p.E * b.m_tiles * b.n_tiles, s);
+  CUtensorMap oW2, oW1, oW3;  // fp32 outputs, 32 x 32 boxes: dW2 [E][h'][d_ff]; dW1, dW3 [E][d_ff][h']
+  if (!encode_tmap_3d_f32_sw128(&oW2, dw_down, dff, hu, E, 32, 32) ||
+      !encode_tmap_3d_f32_sw128(&oW1, dw_gate, hu, dff, E, 32, 32) ||
+      !encode_tmap_3d_f32_sw128(&oW3, dw_up, hu, dff, E, 32, 32))
+    return cudaErrorInvalidValue;
+  e = launch_bwd<kModeDW>(mDYt, mH, mH, oW2, oW2, b, (int64_t)p.E * b.m_tiles * b.n_tiles, s);
   if (e != cudaSuccess) return e;
 
-  // DW: dW1 | dW3 = (dG | dU)ᵀ·X  ([E][d_ff][h'] each)
-  b.m_total = 2 * p.d_ff;
-  b.m_split = p.d_ff;
-  b.m_tiles = (2 * p.d_ff + kBM - 1) / kBM;
-  b.n_out = p.hu;
-  b.n_tiles = (p.hu + kBN - 1) / kBN;
+  // DW: (dW1 | dW3)ᵀ = Xᵀ·(dG | dU) ([h'][2·d_ff] per expert, stored as dW1, dW3 [E][d_ff][h']):
+  // A = X transposed (K-major), B = dG|dU (MN-major)
+  e = launch_transpose_pad(p, x_packed, offsets, p.hu, pcols, x_t, s);
+  if (e != cudaSuccess) return e;
+  b.m_total = p.hu;
+  b.m_tiles = (p.hu + kBM - 1) / kBM;
+  b.n_out = 2 * p.d_ff;
+  b.n_split = p.d_ff;
+  b.n_tiles = (2 * p.d_ff + kBN - 1) / kBN;
+  b.transposed_out = 1;
   b.out_a = dw_gate;
   b.out_b = dw_up;
-  return launch_bwd<kModeDW>(mDGUm, mX, mX, b, (int64_t)p.E * b.m_tiles * b.n_tiles, s);
+  return launch_bwd<kModeDW>(mXt, mDGUm, mDGUm, oW1, oW3, b, (int64_t)p.E * b.m_tiles * b.n_tiles, s);
 }
 
 }  // namespace moe

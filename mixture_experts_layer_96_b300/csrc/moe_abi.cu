@@ -71,6 +71,19 @@ bool encode_tmap_mn_blocks_bf16(CUtensorMap* map, const void* base, uint64_t col
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tmap_3d_f32_sw128(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                              uint32_t box0, uint32_t box1) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || (reinterpret_cast<uintptr_t>(base) & 15) != 0 || (d0 * 4) % 16 != 0) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 4, d0 * d1 * 4};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 moe_status_t make_problem(const moe_config_t* c, Problem* p) {
   if (!c || !p) return MOE_ERR_INVALID_ARG;
   if (c->T < 0 || c->h < 1 || c->n_heads < 1 || c->h % c->n_heads != 0) return MOE_ERR_INVALID_ARG;
@@ -154,6 +167,8 @@ struct BwdLayout {
   size_t dgate;      // fp32 [T'][K]
   size_t dl;         // fp32 [T'][E]
   size_t wg_part;    // fp32 [chunks][h'][E]
+  size_t dy_t;       // bf16 [h'][padded cols]  dY_packed transposed, experts padded to 64 rows
+  size_t x_t;        // bf16 [h'][padded cols]  X_packed transposed, likewise
   size_t total;
 };
 
@@ -172,6 +187,8 @@ static BwdLayout bwd_layout(const Problem& p) {
   L.dgate = take(TK * 4);
   L.dl = take((size_t)p.Tu * p.E * 4);
   L.wg_part = take((size_t)backward_wg_chunks(p) * p.hu * p.E * 4);
+  L.dy_t = take((size_t)p.hu * (size_t)backward_padded_cols(p) * 2);
+  L.x_t = take((size_t)p.hu * (size_t)backward_padded_cols(p) * 2);
   L.total = off;
   return L;
 }
@@ -397,7 +414,8 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_expert_ffn_backward(p, offsets, ws_ptr<void>(ws, L.x_packed), ws_ptr<void>(ws, L.hidden), gu,
                                  dy_packed, w->w_gate, w->w_up, w->w_down, dgu, dx_packed, grads->dw_gate,
-                                 grads->dw_up, grads->dw_down, status, s);
+                                 grads->dw_up, grads->dw_down, ws_ptr<void>(bws, B.dy_t), ws_ptr<void>(bws, B.x_t),
+                                 status, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_backward_router(p, x, dl, backward_wg_chunks(p), ws_ptr<float>(bws, B.wg_part), grads->dw_router, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;

@@ -87,6 +87,11 @@ bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uin
 bool encode_tmap_mn_blocks_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                                 uint32_t box_rows, uint32_t blocks);
 
+// fp32 [d2][d1][d0] tensor (d0 contiguous) with a {box0, box1, 1} box and 128-byte swizzle
+// (box0·4 must be 128 bytes or less): the target of tiled stores from swizzled shared memory.
+bool encode_tmap_3d_f32_sw128(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                              uint32_t box0, uint32_t box1);
+
 // ---- launchers (return cudaSuccess or the launch error) --------------------------------------
 cudaError_t launch_route(const Problem& p, const void* x, const void* w_router,
                          const float* logits_in, const float* logit_bias, const float* select_bias,
@@ -111,7 +116,8 @@ cudaError_t launch_expert_ffn_backward(const Problem& p, const int32_t* offsets,
                                        const void* hidden, const void* gu, const void* dy_packed,
                                        const void* w_gate, const void* w_up, const void* w_down,
                                        void* dgu, void* dx_packed, float* dw_gate, float* dw_up,
-                                       float* dw_down, uint32_t* status, cudaStream_t s);
+                                       float* dw_down, void* dy_t, void* x_t, uint32_t* status, cudaStream_t s);
+int64_t backward_padded_cols(const Problem& p);  // columns of the padded transposed copies
 cudaError_t launch_backward_misc_combine(const Problem& p, const void* dy, const void* y_packed,
                                          const int32_t* slot_of, const float* gate, void* dy_packed,
                                          float* dgate, uint32_t* status, cudaStream_t s);
