@@ -116,49 +116,54 @@ __global__ void bwd_logits_kernel(const float* __restrict__ logits, const int32_
   }
 }
 
-// dW_g partials: block (i-tile of 64, e-tile of 64, token chunk) → part[chunk][i][e] = Σ_t x[t][i]·dl[t][e].
-constexpr int kWgTile = 64, kWgT = 32;
-__global__ void __launch_bounds__(256) bwd_wg_partial_kernel(const __nv_bfloat16* __restrict__ x,
+// dW_g partials: part[chunk][i][e] = Σ_{t in chunk} x[t][i]·dl[t][e]. A block covers 256 columns i
+// (two per thread, one bf16x2 load per token) and EC experts (the thread's accumulators), its
+// tokens' dl rows staged in shared memory; x is read once per expert chunk, coalesced.
+constexpr int kWgCols = 256, kWgT = 64;
+template <int EC>
+__global__ void __launch_bounds__(128) bwd_wg_partial_kernel(const __nv_bfloat16* __restrict__ x,
                                                              const float* __restrict__ dl, int64_t Tu, int hu,
                                                              int E, int64_t chunk_len, float* __restrict__ part) {
-  __shared__ float sx[kWgT][kWgTile + 1];
-  __shared__ float sd[kWgT][kWgTile + 1];
-  const int i0 = blockIdx.x * kWgTile, e0 = blockIdx.y * kWgTile;
+  __shared__ float sd[kWgT][EC];
+  const int i = blockIdx.x * kWgCols + 2 * threadIdx.x;
+  const int e0 = blockIdx.y * EC;
   const int64_t t_begin = (int64_t)blockIdx.z * chunk_len;
   const int64_t t_end = t_begin + chunk_len < Tu ? t_begin + chunk_len : Tu;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 x 16 threads, 4 x 4 outputs each
-  float acc[4][4] = {};
+  float a0[EC], a1[EC];
+#pragma unroll
+  for (int j = 0; j < EC; ++j) a0[j] = a1[j] = 0.0f;
   for (int64_t t0 = t_begin; t0 < t_end; t0 += kWgT) {
-    for (int j = threadIdx.x; j < kWgT * kWgTile; j += 256) {
-      const int r = j / kWgTile, c = j % kWgTile;
+    __syncthreads();
+    for (int j = threadIdx.x; j < kWgT * EC; j += 128) {
+      const int r = j / EC, c = j % EC;
       const int64_t t = t0 + r;
-      sx[r][c] = (t < t_end && i0 + c < hu) ? __bfloat162float(x[t * hu + i0 + c]) : 0.0f;
       sd[r][c] = (t < t_end && e0 + c < E) ? dl[t * E + e0 + c] : 0.0f;
     }
     __syncthreads();
-#pragma unroll 4
-    for (int r = 0; r < kWgT; ++r) {
-      float a[4], b[4];
+    const int n = (int)(t_end - t0 < kWgT ? t_end - t0 : kWgT);
+    if (i < hu) {
+#pragma unroll 2
+      for (int r = 0; r < n; ++r) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(x + (t0 + r) * hu + i);
+        const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        a[j] = sx[r][ty * 4 + j];
-        b[j] = sd[r][tx * 4 + j];
+        for (int j = 0; j < EC; ++j) {
+          a0[j] = fmaf(x0, sd[r][j], a0[j]);
+          a1[j] = fmaf(x1, sd[r][j], a1[j]);
+        }
       }
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-#pragma unroll
-        for (int n = 0; n < 4; ++n) acc[m][n] = fmaf(a[m], b[n], acc[m][n]);
     }
-    __syncthreads();
   }
-  float* out = part + (int64_t)blockIdx.z * hu * E;
+  if (i < hu) {
+    float* out = part + (int64_t)blockIdx.z * hu * E;
 #pragma unroll
-  for (int m = 0; m < 4; ++m)
-#pragma unroll
-    for (int n = 0; n < 4; ++n) {
-      const int i = i0 + ty * 4 + m, e = e0 + tx * 4 + n;
-      if (i < hu && e < E) out[(int64_t)i * E + e] = acc[m][n];
+    for (int j = 0; j < EC; ++j) {
+      if (e0 + j < E) {
+        out[(int64_t)i * E + e0 + j] = a0[j];
+        out[(int64_t)(i + 1) * E + e0 + j] = a1[j];
+      }
     }
+  }
 }
 
 __global__ void bwd_wg_reduce_kernel(const float* __restrict__ part, int nchunks, int64_t n, float* __restrict__ dwg) {
@@ -195,6 +200,7 @@ __global__ void bwd_dx_kernel(const uint4* __restrict__ dx_packed, const int32_t
         for (int j = 0; j < 8; ++j) acc[j] += f[j];
       }
     }
+#pragma unroll 8
     for (int e = 0; e < E; ++e) {
       float f[8];
       bf16x8_to_f32(wgt[(int64_t)e * vecs + v], f);
@@ -236,11 +242,12 @@ cudaError_t launch_backward_logits(const Problem& p, const float* logits, const 
   return cudaGetLastError();
 }
 
-// Chunks of the token range for the dW_g partials: about 512 blocks (several per SM on a B300),
+// Chunks of the token range for the dW_g partials: about 600 blocks (four per SM on a B300),
 // fixed by the config alone so that the backward workspace size needs no device query.
+static int wg_expert_chunk(const Problem& p) { return p.E <= 8 ? 8 : 16; }
 int backward_wg_chunks(const Problem& p) {
-  const int64_t tiles = (int64_t)((p.hu + kWgTile - 1) / kWgTile) * ((p.E + kWgTile - 1) / kWgTile);
-  int64_t c = (512 + tiles - 1) / tiles;
+  const int64_t tiles = (int64_t)((p.hu + kWgCols - 1) / kWgCols) * ((p.E + wg_expert_chunk(p) - 1) / wg_expert_chunk(p));
+  int64_t c = (600 + tiles - 1) / tiles;
   const int64_t max_c = (p.Tu + kWgT - 1) / kWgT;
   if (c > max_c) c = max_c;
   if (c < 1) c = 1;
@@ -253,10 +260,11 @@ cudaError_t launch_backward_router(const Problem& p, const void* x, const float*
   const int64_t n = (int64_t)p.hu * p.E;
   if (p.Tu == 0) return cudaMemsetAsync(dw_router, 0, (size_t)n * 4, s);
   int64_t chunk_len = (p.Tu + nchunks - 1) / nchunks;
-  chunk_len = (chunk_len + kWgT - 1) / kWgT * kWgT;
-  const dim3 grid((p.hu + kWgTile - 1) / kWgTile, (p.E + kWgTile - 1) / kWgTile, (unsigned)nchunks);
-  bwd_wg_partial_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), dl, p.Tu, p.hu, p.E, chunk_len,
-                                             part);
+  const int ec = wg_expert_chunk(p);
+  const dim3 grid((p.hu + kWgCols - 1) / kWgCols, (p.E + ec - 1) / ec, (unsigned)nchunks);
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  if (ec == 8) bwd_wg_partial_kernel<8><<<grid, 128, 0, s>>>(xb, dl, p.Tu, p.hu, p.E, chunk_len, part);
+  else bwd_wg_partial_kernel<16><<<grid, 128, 0, s>>>(xb, dl, p.Tu, p.hu, p.E, chunk_len, part);
   note_launch();
   bwd_wg_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(part, nchunks, n, dw_router);
   note_launch();

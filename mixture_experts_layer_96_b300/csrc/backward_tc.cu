@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(256) transpose_pad_kernel(const __nv_bfloat16*
                                                             __nv_bfloat16* __restrict__ out) {
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_pre[kMaxExperts + 1];
-  __shared__ __align__(16) uint16_t tile[64][64 + 8];  // [row k][column i]
+  __shared__ __align__(16) uint16_t tile[64][64 + 2];  // [row k][column i]; 33-word rows: few bank conflicts
   __shared__ int s_ok;
   if (threadIdx.x < 32) {
     const bool ok = warp_tile_prefix(offsets, E, 64, rows_cap, s_off, s_pre);
@@ -427,7 +427,11 @@ __global__ void __launch_bounds__(256) transpose_pad_kernel(const __nv_bfloat16*
     const int k = j >> 3, v = j & 7;
     uint4 val = make_uint4(0u, 0u, 0u, 0u);
     if (k < valid && i0 + v * 8 < cols) val = *reinterpret_cast<const uint4*>(in + (int64_t)(r0 + k) * cols + i0 + v * 8);
-    *reinterpret_cast<uint4*>(&tile[k][v * 8]) = val;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(&tile[k][v * 8]);
+    dst[0] = val.x;
+    dst[1] = val.y;
+    dst[2] = val.z;
+    dst[3] = val.w;
   }
   __syncthreads();
   for (int j = threadIdx.x; j < 64 * 8; j += 256) {
