@@ -118,14 +118,6 @@ __device__ __forceinline__ void bulk_wait_group_read0() { asm volatile("cp.async
 // Wait until the committed bulk stores are complete.
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                                 int32_t x, int32_t y, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
-      : "memory");
-}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -204,8 +196,8 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t
   return d;
 }
 
-// Instruction-descriptor bits marking A / B as MN-major (transposed) operands.
-constexpr uint32_t kIdescAMajorMN = 1u << 15;
+// Instruction-descriptor bit marking B as an MN-major (transposed) operand (bit 15 does the same
+// for A).
 constexpr uint32_t kIdescBMajorMN = 1u << 16;
 
 // Make this thread's generic-proxy shared-memory writes visible to the tensor core (async proxy).
