@@ -15,9 +15,10 @@
 //           expert's rows. A comes K-major from a transposed copy of packed rows in which every
 //           expert's rows start at a multiple of 64 and are zero-padded to one (an MN-major A ran
 //           at about half the tensor rate); B is packed rows read MN-major. B's last k-block
-//           usually extends into the next expert's rows: the MMA warp's 32 lanes zero those K rows
-//           in shared memory before the MMA (then a proxy fence), so no non-finite leftover can
-//           meet A's zero padding. An expert without rows gets a zero tile. dW1|dW3 come out
+//           usually extends into the next expert's rows, which A's zero padding cancels exactly;
+//           where it runs past the last packed row, the MMA warp's 32 lanes zero those K rows in
+//           shared memory before the MMA (then a proxy fence), so no stale non-finite value can
+//           meet the padding. An expert without rows gets a zero tile. dW1|dW3 come out
 //           transposed (M = h', N = 2·d_ff) and are stored row by row of the weight.
 //   warp 0     TMA producer (one lane)
 //   warp 1     TMEM allocator + MMA issuer (lane 0 issues; all lanes zero K tails in DW)
@@ -202,7 +203,10 @@ expert_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         const uint32_t sa = sbase + stage * kStageBytes, sb = sa + kABytes;
         if (MODE == kModeDW) {
           const int valid = s_off[e + 1] - s_off[e] - kb * kBK;
-          if (valid < kBK) {
+          // Rows past the expert meet A's zero padding, so they add exactly 0 while they hold
+          // finite data: the next experts' rows do. Only a block that runs past the last packed
+          // row (where the buffer holds whatever was there) gets those rows zeroed.
+          if (valid < kBK && s_off[e] + (kb + 1) * kBK > s_off[p.E]) {
             // zero K rows valid..63 of the 4 B boxes (one 128-byte row each)
             const int nrow = (kBK - valid) * (kBN / 64);
             for (int i = lane; i < nrow * 8; i += 32) {
