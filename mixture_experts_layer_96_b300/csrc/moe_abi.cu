@@ -366,7 +366,9 @@ moe_status_t moe_forward_train(const moe_config_t* cfg, const void* x, const moe
   const moe_status_t st = make_problem(cfg, &p);
   if (st != MOE_OK) return st;
   if (!backward_supported(p)) return MOE_ERR_UNSUPPORTED;
-  if (!out || !out->topk_idx || !out->topk_gate || !out->logits || !out->slot_of) return MOE_ERR_INVALID_ARG;
+  // the per-unit outputs the backward reads (empty, possibly NULL, when there are no units)
+  if (!out || (p.Tu > 0 && (!out->topk_idx || !out->topk_gate || !out->logits || !out->slot_of)))
+    return MOE_ERR_INVALID_ARG;
   if (p.rows > 0 && (!gu || !aligned16(gu))) return MOE_ERR_INVALID_ARG;
   return forward_impl(cfg, x, w, y, out, ws, stream, gu);
 }
@@ -386,8 +388,10 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
   if (!backward_supported(p)) return MOE_ERR_UNSUPPORTED;
   if (!ws_ok(ws) || !ws_ok(bws)) return MOE_ERR_WORKSPACE;
   if (!w || !w->w_router || !w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
-  if (!out || !out->topk_idx || !out->topk_gate || !out->logits || !out->slot_of) return MOE_ERR_INVALID_ARG;
-  if (!grads || !grads->dx || !grads->dw_router || !grads->dw_gate || !grads->dw_up || !grads->dw_down)
+  if (!out || (p.Tu > 0 && (!out->topk_idx || !out->topk_gate || !out->logits || !out->slot_of)))
+    return MOE_ERR_INVALID_ARG;
+  if (!grads || (p.Tu > 0 && !grads->dx) || !grads->dw_router || !grads->dw_gate || !grads->dw_up ||
+      !grads->dw_down)
     return MOE_ERR_INVALID_ARG;
   if (!isfinite(d_aux)) return MOE_ERR_INVALID_ARG;
   if (p.Tu > 0 && (!x || !dy || !gu)) return MOE_ERR_INVALID_ARG;

@@ -40,6 +40,7 @@ SMALL = [
     MoEShape("odd_tiles", T=300, h=192, E=5, K=2, d_ff=192, capacity_factor=0.9),           # partial M/N tiles
     MoEShape("sparse_experts", T=20, h=128, E=16, K=1, d_ff=128),                           # empty experts
     MoEShape("switch_top1", T=600, h=128, E=8, K=1, d_ff=256, capacity_factor=1.2, logit_bias="zipf1.2"),
+    MoEShape("drop_heavy", T=500, h=128, E=4, K=2, d_ff=128, capacity_factor=0.3, logit_bias="zipf1.2"),
 ]
 
 
@@ -146,6 +147,23 @@ def test_forward_train_equals_forward_and_saves_the_swiglu_inputs():
             U = widen(inp.w3[e], True) @ xu[t]
             want = np.concatenate([G, U])
             assert np.max(np.abs(gu64[r] - want)) <= 2 ** -8 * np.max(np.abs(want)) + 1e-3
+
+
+def test_backward_empty_batch():
+    """T = 0: nothing to route; the weight gradients are zero and every call succeeds."""
+    shape = MoEShape("empty", T=0, h=128, E=8, K=2, d_ff=128)
+    cfg = config_of(shape)
+    inp = Inputs.make(scaled(shape, T=1))
+    _, lw = inp.device()
+    x = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
+    ws = Workspace(cfg)
+    outs = ForwardOutputs.allocate(cfg, "cuda")
+    y, gu = moe_forward_train(cfg, x, lw, outs, ws=ws)
+    g = moe_backward(cfg, x, lw, torch.empty_like(x), outs, gu, ws=ws, bws=BackwardWorkspace(cfg), d_aux=1.0)
+    ws.check()
+    assert g.dx.shape == (0, 128)
+    for name in ("dw_router", "dw_gate", "dw_up", "dw_down"):
+        assert int(torch.count_nonzero(getattr(g, name))) == 0, name
 
 
 def test_backward_is_deterministic():
