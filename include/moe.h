@@ -181,8 +181,9 @@ MOE_API size_t moe_saved_gu_size(const moe_config_t* cfg);
 /* moe_forward, and also the SwiGLU inputs G = X_e·W1_eᵀ and U = X_e·W3_eᵀ of every kept packed
  * row, bf16, into gu [T'·K][2·d_ff] (G in columns [0, d_ff), U in [d_ff, 2·d_ff)).
  * `out` is required, with topk_idx, topk_gate, logits and slot_of non-NULL when T' > 0 (the
- * backward reads them). Keep `ws`, `out` and `gu` unchanged until moe_backward has run: the backward also reads
- * the forward's packed rows, hidden activations and expert outputs from `ws`. */
+ * backward reads them); gu must be 16-byte aligned. Keep `ws`, `out` and `gu` unchanged until
+ * moe_backward has run: the backward also reads the forward's packed rows, hidden activations
+ * and expert outputs from `ws`. */
 MOE_API moe_status_t moe_forward_train(const moe_config_t* cfg, const void* x, const moe_weights_t* w,
                                        void* y, const moe_outputs_t* out, void* gu, void* ws,
                                        moe_stream_t stream);
@@ -204,8 +205,9 @@ MOE_API size_t moe_backward_workspace_size(const moe_config_t* cfg);
 /* Backward of the moe_forward_train call that filled `ws`, `out` and `gu` for this x and w.
  *  dy [T][h] bf16: dL/dy. d_aux: weight of L_aux in L (host float).
  *  Out: every member of `grads` except dlogits/dgate is required (dx only when T' > 0); dw_* are
- *  overwritten (not accumulated). Deterministic: the same inputs give the same bits. Errors as for moe_forward;
- *  kernel faults set the status word of `ws`. */
+ *  overwritten (not accumulated). x, dy, gu, dx, the expert weights and dw_* must be 16-byte
+ *  aligned; bws 256-byte aligned. Deterministic: the same inputs give the same bits. Errors as
+ *  for moe_forward; kernel faults set the status word of `ws`. */
 MOE_API moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weights_t* w,
                                   const void* dy, float d_aux, const moe_outputs_t* out, const void* gu,
                                   void* ws, const moe_grads_t* grads, void* bws, moe_stream_t stream);
