@@ -82,6 +82,54 @@ def choose_peak(pk: dict, clocks: dict):
     return float(pk["bf16_tflops"]), f"bf16 burst ({pk['source']})"
 
 
+SPEC_BF16_TFLOPS = 2250.0  # B300 dense bf16, nominal
+
+
+def gemm_bytes(shape, kept: int, e_active: int) -> float:
+    """HBM bytes of the expert GEMMs of one forward: the active experts' weights once, plus the
+    activations (x_packed read, H written and read back, y_packed written)."""
+    s = 2 if shape.dtype == "bf16" else 4
+    weights = 3.0 * e_active * shape.h_unit * shape.d_ff * s
+    acts = kept * (shape.h_unit + 2 * shape.d_ff + shape.h_unit) * s
+    return weights + acts
+
+
+def layer_roofline(shape, kept: int, e_active: int, stage_ms: dict, ms_per_forward: float, hbm_gbs: float,
+                   gemm_peak_tf: float) -> dict:
+    """Each stage's time at its roofline and the forward's fraction of their sum.
+
+    route: x, W_g and the picks at HBM rate, or the router FLOP at the tensor peak if that is
+    longer; dispatch and combine: their bytes at HBM rate; expert GEMMs: the longer of FLOP at the
+    tensor peak and weight + activation bytes at HBM rate (that choice names the GEMMs' bound).
+    """
+    s = 2 if shape.dtype == "bf16" else 4
+    Tu, hu, E, K = shape.T_units, shape.h_unit, shape.E, shape.K
+    bw = hbm_gbs * 1e9
+    pk = gemm_peak_tf * 1e12
+    route = max((Tu * hu * s + hu * E * s + Tu * K * 8) / bw, 2.0 * Tu * hu * E / pk)
+    dispatch = (Tu * hu * s + kept * hu * s + kept * 8) / bw
+    combine = (kept * hu * s + Tu * hu * s + Tu * K * 8) / bw
+    t_flop = 6.0 * hu * shape.d_ff * kept / pk
+    t_bytes = gemm_bytes(shape, kept, e_active) / bw
+    ffn = max(t_flop, t_bytes)
+    roof = {"route": route, "dispatch": dispatch, "expert_ffn": ffn, "combine": combine}
+    total = sum(roof.values())
+    out = {f"{k}_ms_at_roofline": 1e3 * v for k, v in roof.items()}
+    out.update({
+        "sum_ms_at_roofline": 1e3 * total,
+        "forward_ms": ms_per_forward,
+        "frac_of_forward": 1e3 * total / ms_per_forward if ms_per_forward > 0 else None,
+        "gemm_bound": "tensor" if t_flop >= t_bytes else "hbm",
+        "stage_frac": {k: 1e3 * roof[k] / stage_ms[k] for k in roof if stage_ms.get(k)},
+        "peaks": {"hbm_gbs": hbm_gbs, "bf16_tflops": gemm_peak_tf},
+    })
+    return out
+
+
+def median(values) -> float:
+    return float(statistics.median(values)) if values else 0.0
+
+
 def aggregate_max(value: float, world: int, device=None) -> float:
     """Max of a per-rank value over all ranks (the slowest rank sets the step)."""
     if world <= 1:
@@ -250,8 +298,18 @@ def cpu_baseline_leg(shape, n_sample):
     run = OracleRun(shape, min(n_sample, shape.T_units))
     t_route, per_unit = run.step()
     v = shape.T / run.full_batch_seconds(t_route, per_unit)
-    return {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": run.describe(t_route, per_unit)}
+    out = {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+           "sample": run.describe(t_route, per_unit)}
+    if shape.dtype == "f32":  # the small layer: also the oracle on one core
+        try:
+            from threadpoolctl import threadpool_limits
+            with threadpool_limits(1):
+                t1, pu1 = run.step()
+            out["single_core_value"] = shape.T / run.full_batch_seconds(t1, pu1)
+        except Exception as ex:  # a report extra: never lose the line for it
+            out["single_core_value"] = None
+            out["single_core_error"] = repr(ex)
+    return out
 
 
 # ------------------------------------------------------------------------------------ reference arm
@@ -428,7 +486,9 @@ def run_ours(args, shape):
     barrier()
     t1 = time.time()
     n_launch = (per_forward * args.steps) if graph is not None else (launch_count() - n0)
-    ms = aggregate_max(sum(a.elapsed_time(b) for a, b in ev) / args.steps, world, device)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = aggregate_max(sum(step_ms) / args.steps, world, device)
+    ms_median = aggregate_max(median(step_ms), world, device)
     ws.check()
 
     # ---- per-stage events (same kernels through the stage entry points)
@@ -568,6 +628,24 @@ def run_ours(args, shape):
                        "neighbouring steps overlap this step's compute on two copy streams"},
         "gpu_launches": n_launch,
     }
+    line["ms_per_step_median"] = ms_median
+    line["roofline"]["frac_of_spec"] = achieved_tf / SPEC_BF16_TFLOPS
+    try:  # report extras: on any error the line keeps everything above and says why
+        e_active = sum(1 for c in counts if c > 0)
+        lr = layer_roofline(shape, kept, e_active, stage_ms, ms, hbm, peak_tf)
+        line["layer_roofline"] = lr
+        if lr["gemm_bound"] == "hbm":
+            # the GEMMs stream more weight bytes than their FLOP take at the tensor peak: the HBM
+            # roofline grades them; the tensor view stays in the line
+            gb = gemm_bytes(shape, kept, e_active)
+            ach = gb / (stage_ms["expert_ffn"] * 1e-3) / 1e9
+            tensor_view = dict(line["roofline"])
+            line["roofline"] = {"bound": "hbm", "kernel": tensor_view["kernel"], "achieved": ach, "peak": hbm,
+                                "unit": "GB/s", "frac": ach / hbm, "algorithmic_bytes": gb,
+                                "traffic": tensor_view["traffic"], "traffic_unit": tensor_view["traffic_unit"],
+                                "gemm_source_sha1": tensor_view["gemm_source_sha1"], "tensor_view": tensor_view}
+    except Exception as ex:
+        line["layer_roofline"] = {"error": repr(ex)}
     if train is not None:
         bw_peak = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
         train["backward_frac_of_sustained_whole"] = train["backward_tflops_whole"] / bw_peak

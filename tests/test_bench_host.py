@@ -84,3 +84,54 @@ def test_peak_choice():
     assert bench.choose_peak(pk, {"reasons": [], "sm_mhz": 2032, "sm_max_mhz": 2032})[0] == 1815.6
     assert bench.choose_peak(pk, {"reasons": ["sw_power_cap"], "sm_mhz": 1300, "sm_max_mhz": 2032})[0] == 1413.1
     assert bench.choose_peak(pk, {"reasons": [], "sm_mhz": 1000, "sm_max_mhz": 2032})[0] == 1413.1
+
+
+def test_gemm_bytes_by_hand():
+    s = bench.WORKLOADS["mixtral_bf16"]
+    kept = s.T_units * s.K
+    w = 3 * 8 * 4096 * 14336 * 2                   # W1, W3, W2 of every expert, bf16
+    a = kept * (4096 + 14336 + 14336 + 4096) * 2     # x_packed, H written and read, y_packed
+    assert bench.gemm_bytes(s, kept, 8) == w + a
+    assert bench.gemm_bytes(s, kept, 3) - bench.gemm_bytes(s, kept, 2) == 3 * 4096 * 14336 * 2
+
+
+def test_layer_roofline_dense_workload_is_tensor_bound():
+    s = bench.WORKLOADS["mixtral_bf16"]
+    kept = s.T_units * s.K
+    stage = {"route": 0.02, "dispatch": 0.03, "expert_ffn": 2.2, "combine": 0.04}
+    lr = bench.layer_roofline(s, kept, 8, stage, 2.35, 7000.0, 1413.0)
+    assert lr["gemm_bound"] == "tensor"
+    t_ffn = 6.0 * 4096 * 14336 * kept / 1413e12
+    assert lr["expert_ffn_ms_at_roofline"] == pytest.approx(1e3 * t_ffn)
+    # dispatch: x read, x_packed written, 8 B of slot bookkeeping per kept row
+    assert lr["dispatch_ms_at_roofline"] == pytest.approx(1e3 * (4096 * 4096 * 2 * 3 + kept * 8) / 7e12)
+    parts = [lr[f"{k}_ms_at_roofline"] for k in ("route", "dispatch", "expert_ffn", "combine")]
+    assert lr["sum_ms_at_roofline"] == pytest.approx(sum(parts))
+    assert lr["frac_of_forward"] == pytest.approx(lr["sum_ms_at_roofline"] / 2.35)
+    assert lr["stage_frac"]["expert_ffn"] == pytest.approx(1e3 * t_ffn / 2.2)
+    assert 0.8 < lr["frac_of_forward"] < 1.0
+
+
+def test_layer_roofline_fine_grained_workload_streams_weights():
+    """256 experts of d_ff 2048 at T = 4096: each expert's weights are read for ~128 rows, so the
+    GEMMs take longer to stream their weights from HBM than to do their FLOP."""
+    s = bench.WORKLOADS["finegrained_bf16"]
+    kept = s.T_units * s.K
+    stage = {"route": 0.03, "dispatch": 0.1, "expert_ffn": 4.8, "combine": 0.1}
+    lr = bench.layer_roofline(s, kept, 256, stage, 5.03, 7000.0, 1413.0)
+    assert lr["gemm_bound"] == "hbm"
+    assert lr["expert_ffn_ms_at_roofline"] == pytest.approx(1e3 * bench.gemm_bytes(s, kept, 256) / 7e12)
+    # with few experts active the weight stream shrinks below the FLOP time
+    assert bench.layer_roofline(s, kept, 16, stage, 5.03, 7000.0, 1413.0)["gemm_bound"] == "tensor"
+
+
+def test_median_of_step_times():
+    assert bench.median([3.0, 1.0, 2.0]) == 2.0
+    assert bench.median([4.0, 1.0, 2.0, 3.0]) == 2.5
+    assert bench.median([]) == 0.0
+
+
+def test_cpu_baseline_adds_a_single_core_time_for_the_f32_layer():
+    cb = bench.cpu_baseline_leg(bench.WORKLOADS["tiny_f32"], 8)
+    assert cb["kind"] == "oracle" and cb["value"] > 0
+    assert cb["single_core_value"] is not None and cb["single_core_value"] > 0
