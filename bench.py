@@ -291,7 +291,11 @@ def blas_threads():
         n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
         return int(max(n)) if n else 1
     except Exception:
-        return os.cpu_count() or 1
+        # without threadpoolctl: an explicit BLAS thread setting, else the cores this process may use
+        for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            if os.environ.get(k, "").isdigit():
+                return int(os.environ[k])
+        return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
 
 
 def cpu_baseline_leg(shape, n_sample):
@@ -302,14 +306,31 @@ def cpu_baseline_leg(shape, n_sample):
            "sample": run.describe(t_route, per_unit)}
     if shape.dtype == "f32":  # the small layer: also the oracle on one core
         try:
-            from threadpoolctl import threadpool_limits
-            with threadpool_limits(1):
-                t1, pu1 = run.step()
-            out["single_core_value"] = shape.T / run.full_batch_seconds(t1, pu1)
+            out["single_core_value"] = single_core_oracle(shape.name, n_sample)
         except Exception as ex:  # a report extra: never lose the line for it
             out["single_core_value"] = None
             out["single_core_error"] = repr(ex)
     return out
+
+
+def oracle_tokens_per_s(name: str, n_sample: int) -> float:
+    shape = WORKLOADS[name]
+    run = OracleRun(shape, min(n_sample, shape.T_units))
+    t_route, per_unit = run.step()
+    return shape.T / run.full_batch_seconds(t_route, per_unit)
+
+
+def single_core_oracle(name: str, n_sample: int, timeout_s: float = 300.0) -> float:
+    """The oracle's tokens/s with its BLAS held to one thread: a fresh interpreter (the thread
+    count is fixed when numpy loads) that sees no GPU."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    for k in ("RANK", "LOCAL_RANK", "WORLD_SIZE"):
+        env.pop(k, None)
+    code = f"import bench; print(bench.oracle_tokens_per_s({name!r}, {int(n_sample)}))"
+    r = subprocess.run([sys.executable, "-c", code], cwd=os.path.dirname(os.path.abspath(__file__)), env=env,
+                       capture_output=True, text=True, timeout=timeout_s, check=True)
+    return float(r.stdout.strip().splitlines()[-1])
 
 
 # ------------------------------------------------------------------------------------ reference arm
