@@ -195,3 +195,39 @@ def test_entry_oracle_equals_the_whole_gradient(cfg):
     for key, at, full in (("dw2", at2, g.dw2), ("dw1", at1, g.dw1), ("dw3", at3, g.dw3)):
         for a in at:
             assert r[key][a] == pytest.approx(full[a], rel=1e-12, abs=1e-14)
+
+
+def fd_fails_on(monkeypatch, target, replacement, cfg, name):
+    """True when, with B.<target> replaced, the oracle's gradient in `name` along a random
+    direction disagrees with central differences of the (unpatched) forward oracle."""
+    monkeypatch.setattr(B, target, replacement)
+    p, kw = case_for(cfg)
+    g = grads_of(p, kw)
+    rng = np.random.default_rng(13)
+    v = rng.standard_normal(p[name].shape)
+    eps = 1e-6
+    pp = dict(p); pm = dict(p)
+    pp[name] = p[name] + eps * v
+    pm[name] = p[name] - eps * v
+    fd = (loss(pp, kw, g.idx) - loss(pm, kw, g.idx)) / (2 * eps)
+    return float(np.sum(getattr(g, NAMES[name]) * v)) != pytest.approx(fd, rel=1e-6, abs=1e-8)
+
+
+def test_pin_catches_a_swiglu_derivative_with_a_flipped_sigmoid(monkeypatch):
+    wrong = lambda z: 1.0 / (1.0 + np.exp(z))  # σ(−z) in place of σ(z)
+    cfg = dict(E=6, K=2, score="softmax")
+    assert fd_fails_on(monkeypatch, "sigmoid", wrong, cfg, "w1")
+
+
+def test_pin_catches_a_dx_without_the_router_path(monkeypatch):
+    # drop dL/dl (gates and aux) entirely: dx loses its W_g term, dW_g becomes zero
+    cfg = dict(E=6, K=2, score="sigmoid")
+    monkeypatch.setattr(B, "aux_backward", lambda l, *a: np.zeros(l.shape))
+    assert fd_fails_on(monkeypatch, "gate_backward", lambda l, *a: np.zeros(l.shape), cfg, "x")
+
+
+def test_pin_catches_gradients_that_ignore_capacity_drops(monkeypatch):
+    cfg = dict(E=6, K=2, score="softmax", capacity_factor=0.5)
+    p, kw = case_for(cfg)
+    assert (grads_of(p, kw).slot_of < 0).any()  # this case drops picks
+    assert fd_fails_on(monkeypatch, "capacity", lambda *a: None, cfg, "w2")
