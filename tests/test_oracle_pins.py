@@ -178,14 +178,18 @@ def test_dispatch_bruteforce():
     check_dispatch_bruteforce(O)
 
 
-def test_capacity_values():
+def check_capacity_values(mod):
     # C = CF·K·T/E from the capacity passage; the two dropping workloads give integers.
-    assert O.capacity(1.25, 2, 256, 8) == 80
-    assert O.capacity(1.25, 2, 16384, 64) == 640
-    assert O.capacity(None, 2, 256, 8) is None
-    assert O.capacity(0.0, 2, 256, 8) is None
-    assert O.capacity(float("inf"), 2, 256, 8) is None
-    assert O.capacity(1.2, 2, 256, 8) == 77  # 76.8 rounds up
+    assert mod.capacity(1.25, 2, 256, 8) == 80
+    assert mod.capacity(1.25, 2, 16384, 64) == 640
+    assert mod.capacity(None, 2, 256, 8) is None
+    assert mod.capacity(0.0, 2, 256, 8) is None
+    assert mod.capacity(float("inf"), 2, 256, 8) is None
+    assert mod.capacity(1.2, 2, 256, 8) == 77  # 76.8 rounds up
+
+
+def test_capacity_values():
+    check_capacity_values(O)
 
 
 def test_capacity_one_keeps_first_unit():
@@ -313,8 +317,9 @@ def test_silu_closed_form():
     assert O.silu(np.array([0.0]))[0] == 0.0
 
 
-def test_head_split_equals_per_head_layers():
+def check_head_split(mod):
     # H = 2 with no drop: each head slice is an independent layer on [T][h'].
+    O = mod
     rng = np.random.default_rng(8)
     T, hu, E, K, H = 6, 4, 4, 2, 2
     x = rng.standard_normal((T, H * hu))
@@ -327,6 +332,20 @@ def test_head_split_equals_per_head_layers():
         np.testing.assert_allclose(r.y[:, j * hu:(j + 1) * hu], rj.y, rtol=1e-13)
     # sub-token order is t·H + j
     np.testing.assert_allclose(r.logits[1], x[0, hu:] @ wg, rtol=1e-13)
+
+
+def test_head_split_equals_per_head_layers():
+    check_head_split(O)
+
+
+def check_full_drop(mod):
+    # capacity 1 with all units on one expert: only unit 0 keeps its pick.
+    x = np.ones((4, 3))
+    wg = np.zeros((3, 2)); wg[:, 0] = 1.0
+    W = np.ones((2, 5, 3)); W2 = np.ones((2, 3, 5))
+    r = mod.forward(x, wg, lambda e: (W[e], W[e], W2[e]), E=2, K=1, capacity_factor=0.5)
+    assert r.C == 1
+    assert (r.y[1:] == 0).all() and (r.y[0] != 0).all()
 
 
 def test_permutation_equivariance():
@@ -350,13 +369,7 @@ def test_sampled_forward_matches_full():
 
 
 def test_full_drop_gives_zero():
-    # capacity 1 with all units on one expert: only unit 0 keeps its pick.
-    x = np.ones((4, 3))
-    wg = np.zeros((3, 2)); wg[:, 0] = 1.0
-    W = np.ones((2, 5, 3)); W2 = np.ones((2, 3, 5))
-    r = O.forward(x, wg, lambda e: (W[e], W[e], W2[e]), E=2, K=1, capacity_factor=0.5)
-    assert r.C == 1
-    assert (r.y[1:] == 0).all() and (r.y[0] != 0).all()
+    check_full_drop(O)
 
 
 def test_comm_volume():
@@ -395,6 +408,10 @@ MUTANTS = [
     ("aux post-softmax of picks", "routing_probs", lambda l, s: np.full(l.shape, 1.0 / l.shape[1]), check_aux_hand),
     ("topk ties to higher index", "topk", _topk_ties_high, check_topk_bruteforce),
     ("group score = max only", "group_limit", _group_limit_max_only, check_group_bruteforce),
+    ("head-major sub-tokens", "split_heads",
+     lambda x, H: x.reshape(x.shape[0], H, -1).transpose(1, 0, 2).reshape(-1, x.shape[1] // H), check_head_split),
+    ("capacity rounded down", "capacity",
+     lambda cf, K, T, E: None if cf is None else int(math.floor(cf * K * T / E)), check_capacity_values),
     ("gates not renormalised", "gates",
      lambda l, idx, s: np.take_along_axis(scipy.special.softmax(l, axis=1), idx.astype(int), axis=1), check_gates),
 ]
