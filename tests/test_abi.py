@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from mixture_experts_layer_96_b300 import moe as M
 
@@ -112,3 +113,45 @@ def test_backward_rejects_missing_buffers_on_host():
     # the training forward needs the saved outputs
     assert lib.moe_forward_train(ctypes.byref(cfg), 16, ctypes.byref(w), 16, None, 16, 4096, None) \
         == M.MOE_ERR_INVALID_ARG
+
+
+def _weights(cfg, device="cpu", **over):
+    dt, hu, E, F = cfg.torch_dtype, cfg.h_unit, cfg.E, cfg.d_ff
+    t = dict(w_router=torch.empty((hu, E), dtype=dt, device=device),
+             w_gate=torch.empty((E, F, hu), dtype=dt, device=device),
+             w_up=torch.empty((E, F, hu), dtype=dt, device=device),
+             w_down=torch.empty((E, hu, F), dtype=dt, device=device))
+    t.update(over)
+    return M.LayerWeights(**t)
+
+
+def test_binding_rejects_host_tensors_and_wrong_layouts():
+    """The binding hands the library device pointers only: host tensors, wrong shapes and dtypes
+    are refused in Python, before any call into the library. (Checks run shape, dtype, device,
+    contiguity in that order, so host tensors reach the first two.)"""
+    cfg = _cfg(dtype="bf16")
+    bf = torch.bfloat16
+    E, F, hu = cfg.E, cfg.d_ff, cfg.h_unit
+    with pytest.raises(ValueError, match="w_router must be on a CUDA device"):
+        _weights(cfg).check(cfg)
+    with pytest.raises(ValueError, match="w_down: shape"):      # W2 given as [E][d_ff][h']
+        M._req(torch.empty((E, F, hu), dtype=bf), "w_down", (E, hu, F), bf)
+    with pytest.raises(ValueError, match="w_gate: dtype"):
+        M._req(torch.empty((E, F, hu), dtype=torch.float32), "w_gate", (E, F, hu), bf)
+    with pytest.raises(TypeError, match="w_up must be a tensor"):
+        M._req("not a tensor", "w_up", (E, F, hu), bf)
+    with pytest.raises(ValueError, match="w_router: shape"):    # the router weight is [h'][E]
+        _weights(cfg, w_router=torch.empty((E, hu), dtype=bf)).check(cfg)
+
+
+def test_gradient_buffers_are_fp32_except_dx():
+    cfg = _cfg(dtype="bf16")
+    g = M.Grads.allocate(cfg, "cpu")
+    assert g.dx.dtype == torch.bfloat16 and g.dx.shape == (cfg.T, cfg.h)
+    for t in (g.dw_router, g.dw_gate, g.dw_up, g.dw_down, g.dlogits, g.dgate):
+        assert t.dtype == torch.float32
+    assert g.dw_gate.shape == (cfg.E, cfg.d_ff, cfg.h_unit) and g.dw_down.shape == (cfg.E, cfg.h_unit, cfg.d_ff)
+    assert g.dlogits.shape == (cfg.T_units, cfg.E) and g.dgate.shape == (cfg.T_units, cfg.K)
+    with pytest.raises(ValueError, match="CUDA device"):
+        g.check(cfg)
+    assert M.Grads.allocate(cfg, "cpu", extras=False).dlogits is None
