@@ -237,7 +237,12 @@ MOE_API int32_t moe_abi_version(void);
  *  - Limit: 8·ceil(T'/256)·E bytes + about 8·E bytes must fit in 1 MiB (with E = 256, up to
  *    about 130,000 units); larger problems return MOE_ERR_UNSUPPORTED and enqueue nothing.
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
- *    that device current) and keeps it; make that first call before any stream capture.
+ *    that device current) and keeps it; make that first call before any stream capture. Under
+ *    CUDA's lazy module loading (the default that PyTorch sets) that first lookup is also when the
+ *    device reserves the 1 MiB: a caller whose device memory is fixed at start-up should make one
+ *    call (any size, e.g. T = 0) at start-up, while memory is still free.
+ *  - The kept address belongs to the device's context: after cudaDeviceReset (or any teardown of
+ *    the primary context) the library must be reloaded before this call is used again.
  *  - It allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  *  - All calls on a device share the array, which keeps the last call's contents; each call
  *    rewrites every part it reads before reading it, and the one counter in it (zero when the

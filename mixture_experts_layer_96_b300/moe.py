@@ -146,9 +146,38 @@ def launch_count() -> int:
 
 
 # ------------------------------------------------------------------------------------------------
-def _stream(stream) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return s.cuda_stream
+def _stream(stream, device=None) -> int:
+    """Raw handle of `stream`, or of the current stream of `device` (the tensors' device)."""
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if device is not None and stream.device != device:
+        raise ValueError(f"stream is on {stream.device} but the tensors are on {device}")
+    return stream.cuda_stream
+
+
+def _one_device(*tensors) -> torch.device:
+    """The CUDA device every given tensor (None entries skipped) lives on; raises if they differ.
+    The library takes the current device for its per-device state (SM count, static scratch), so
+    every call runs with this device made current."""
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"tensor on {t.device}: every buffer must be on a CUDA device")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"tensors on {dev} and {t.device}: every buffer must be on one device")
+    return dev
+
+
+def _run(tensors, stream, fn, *args) -> int:
+    """Call library function `fn(*args, stream)` with the tensors' device made current (every
+    tensor on that one device, the stream too) and return its status code."""
+    dev = _one_device(*tensors)
+    with torch.cuda.device(dev):
+        return int(fn(*args, _stream(stream, dev)))
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -182,7 +211,7 @@ class Workspace:
         self.nbytes = workspace_size(cfg)
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
         assert self.buf.data_ptr() % 1024 == 0 or self.buf.data_ptr() % 256 == 0
-        _check(load_library().moe_workspace_init(ctypes.byref(cfg), self.ptr, _stream(stream)),
+        _check(_run([self.buf], stream, load_library().moe_workspace_init, ctypes.byref(cfg), self.ptr),
                "moe_workspace_init")
 
     @property
@@ -191,7 +220,7 @@ class Workspace:
 
     def status(self, stream=None) -> int:
         """Wait for the stream; read and clear the device status word."""
-        return int(load_library().moe_get_status(self.ptr, _stream(stream)))
+        return _run([self.buf], stream, load_library().moe_get_status, self.ptr)
 
     def check(self, stream=None):
         _check(self.status(stream), "moe_get_status")
@@ -221,9 +250,9 @@ def moe_route(cfg: MoEConfig, x, w_router, logit_bias=None, select_bias=None, *,
         logits_out = torch.empty((Tu, E), dtype=torch.float32, device=dev)
     if aux_out is None and want_aux:
         aux_out = torch.empty((1,), dtype=torch.float32, device=dev)
-    _check(lib.moe_route(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(select_bias),
-                         _ptr(topk_idx), _ptr(topk_gate), _ptr(logits_out), _ptr(aux_out), ws.ptr,
-                         _stream(stream)), "moe_route")
+    _check(_run([x, w_router, logit_bias, select_bias, topk_idx, topk_gate, logits_out, aux_out, ws.buf], stream,
+                lib.moe_route, ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(select_bias),
+                _ptr(topk_idx), _ptr(topk_gate), _ptr(logits_out), _ptr(aux_out), ws.ptr), "moe_route")
     return topk_idx, topk_gate, logits_out, aux_out
 
 
@@ -240,9 +269,11 @@ def moe_route_logits(cfg: MoEConfig, logits, logit_bias=None, select_bias=None, 
     topk_gate = topk_gate if topk_gate is not None else torch.empty((Tu, K), dtype=torch.float32, device=dev)
     if aux_out is None and want_aux:
         aux_out = torch.empty((1,), dtype=torch.float32, device=dev)
-    _check(lib.moe_route_logits(ctypes.byref(cfg), _ptr(logits), _ptr(logit_bias), _ptr(select_bias),
-                                _ptr(topk_idx), _ptr(topk_gate), _ptr(aux_out), ws.ptr, _stream(stream)),
-           "moe_route_logits")
+    _req(topk_idx, "topk_idx", (Tu, K), torch.int32)
+    _req(topk_gate, "topk_gate", (Tu, K), torch.float32)
+    _check(_run([logits, logit_bias, select_bias, topk_idx, topk_gate, aux_out, ws.buf], stream,
+                lib.moe_route_logits, ctypes.byref(cfg), _ptr(logits), _ptr(logit_bias), _ptr(select_bias),
+                _ptr(topk_idx), _ptr(topk_gate), _ptr(aux_out), ws.ptr), "moe_route_logits")
     return topk_idx, topk_gate, aux_out
 
 
@@ -264,9 +295,9 @@ def moe_dispatch(cfg: MoEConfig, x, topk_idx, *, ws: Workspace, counts=None, off
     _req(slot_of, "slot_of", (Tu, K), torch.int32)
     _req(row_token, "row_token", (Tu * K,), torch.int32)
     _req(x_packed, "x_packed", (Tu * K, hu), dt)
-    _check(lib.moe_dispatch(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts), _ptr(offsets),
-                            _ptr(slot_of), _ptr(row_token), _ptr(x_packed), ws.ptr, _stream(stream)),
-           "moe_dispatch")
+    _check(_run([x, topk_idx, counts, offsets, slot_of, row_token, x_packed, ws.buf], stream, lib.moe_dispatch,
+                ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts), _ptr(offsets), _ptr(slot_of),
+                _ptr(row_token), _ptr(x_packed), ws.ptr), "moe_dispatch")
     return counts, offsets, slot_of, row_token, x_packed
 
 
@@ -283,8 +314,9 @@ def moe_expert_ffn(cfg: MoEConfig, x_packed, offsets, w_gate, w_up, w_down, *, w
     _req(w_down, "w_down", (E, hu, F), dt)
     y_packed = y_packed if y_packed is not None else torch.empty((Tu * K, hu), dtype=dt, device=dev)
     _req(y_packed, "y_packed", (Tu * K, hu), dt)
-    _check(lib.moe_expert_ffn(ctypes.byref(cfg), _ptr(x_packed), _ptr(offsets), _ptr(w_gate), _ptr(w_up),
-                              _ptr(w_down), _ptr(y_packed), ws.ptr, _stream(stream)), "moe_expert_ffn")
+    _check(_run([x_packed, offsets, w_gate, w_up, w_down, y_packed, ws.buf], stream, lib.moe_expert_ffn,
+                ctypes.byref(cfg), _ptr(x_packed), _ptr(offsets), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                _ptr(y_packed), ws.ptr), "moe_expert_ffn")
     return y_packed
 
 
@@ -298,8 +330,8 @@ def moe_combine(cfg: MoEConfig, y_packed, slot_of, topk_gate, *, ws: Workspace, 
     _req(topk_gate, "topk_gate", (Tu, K), torch.float32)
     y = y if y is not None else torch.empty((cfg.T, cfg.h), dtype=dt, device=dev)
     _req(y, "y", (cfg.T, cfg.h), dt)
-    _check(lib.moe_combine(ctypes.byref(cfg), _ptr(y_packed), _ptr(slot_of), _ptr(topk_gate), _ptr(y),
-                           ws.ptr, _stream(stream)), "moe_combine")
+    _check(_run([y_packed, slot_of, topk_gate, y, ws.buf], stream, lib.moe_combine, ctypes.byref(cfg),
+                _ptr(y_packed), _ptr(slot_of), _ptr(topk_gate), _ptr(y), ws.ptr), "moe_combine")
     return y
 
 
@@ -322,6 +354,9 @@ class LayerWeights:
         for b, n in ((self.logit_bias, "logit_bias"), (self.select_bias, "select_bias")):
             if b is not None:
                 _req(b, n, (E,), torch.float32)
+
+    def tensors(self):
+        return (self.w_router, self.w_gate, self.w_up, self.w_down, self.logit_bias, self.select_bias)
 
     def c_struct(self) -> MoEWeights:
         return MoEWeights(_ptr(self.w_router), _ptr(self.logit_bias), _ptr(self.select_bias),
@@ -351,6 +386,9 @@ class ForwardOutputs:
             slot_of=torch.empty((Tu, K), dtype=i32, device=device),
             aux=torch.empty((1,), dtype=f32, device=device))
 
+    def tensors(self):
+        return (self.topk_idx, self.topk_gate, self.logits, self.counts, self.offsets, self.slot_of, self.aux)
+
     def c_struct(self) -> MoEOutputs:
         return MoEOutputs(_ptr(self.topk_idx), _ptr(self.topk_gate), _ptr(self.logits), _ptr(self.counts),
                           _ptr(self.offsets), _ptr(self.slot_of), _ptr(self.aux))
@@ -367,9 +405,9 @@ def moe_forward(cfg: MoEConfig, x, weights: LayerWeights, *, ws: Workspace, y=No
     _req(y, "y", (cfg.T, cfg.h), dt)
     cw = weights.c_struct()
     co = outputs.c_struct() if outputs is not None else None
-    _check(lib.moe_forward(ctypes.byref(cfg), _ptr(x), ctypes.byref(cw), _ptr(y),
-                           ctypes.byref(co) if co is not None else None, ws.ptr, _stream(stream)),
-           "moe_forward")
+    _check(_run([x, y, ws.buf, *weights.tensors(), *(outputs.tensors() if outputs is not None else ())], stream,
+                lib.moe_forward, ctypes.byref(cfg), _ptr(x), ctypes.byref(cw), _ptr(y),
+                ctypes.byref(co) if co is not None else None, ws.ptr), "moe_forward")
     return y
 
 
@@ -394,8 +432,9 @@ def moe_forward_train(cfg: MoEConfig, x, weights: LayerWeights, outputs: Forward
     gu = gu if gu is not None else torch.empty((rows, 2 * cfg.d_ff), dtype=dt, device=x.device)
     _req(gu, "gu", (rows, 2 * cfg.d_ff), dt)
     cw, co = weights.c_struct(), outputs.c_struct()
-    _check(lib.moe_forward_train(ctypes.byref(cfg), _ptr(x), ctypes.byref(cw), _ptr(y), ctypes.byref(co),
-                                 _ptr(gu), ws.ptr, _stream(stream)), "moe_forward_train")
+    _check(_run([x, y, gu, ws.buf, *weights.tensors(), *outputs.tensors()], stream, lib.moe_forward_train,
+                ctypes.byref(cfg), _ptr(x), ctypes.byref(cw), _ptr(y), ctypes.byref(co), _ptr(gu), ws.ptr),
+           "moe_forward_train")
     return y, gu
 
 
@@ -446,6 +485,9 @@ class Grads:
         if self.dgate is not None:
             _req(self.dgate, "dgate", (cfg.T_units, cfg.K), f32)
 
+    def tensors(self):
+        return (self.dx, self.dw_router, self.dw_gate, self.dw_up, self.dw_down, self.dlogits, self.dgate)
+
     def c_struct(self) -> MoEGrads:
         return MoEGrads(_ptr(self.dx), _ptr(self.dw_router), _ptr(self.dw_gate), _ptr(self.dw_up),
                         _ptr(self.dw_down), _ptr(self.dlogits), _ptr(self.dgate))
@@ -464,9 +506,9 @@ def moe_backward(cfg: MoEConfig, x, weights: LayerWeights, dy, outputs: ForwardO
     grads = grads if grads is not None else Grads.allocate(cfg, x.device)
     grads.check(cfg)
     cw, co, cg = weights.c_struct(), outputs.c_struct(), grads.c_struct()
-    _check(lib.moe_backward(ctypes.byref(cfg), _ptr(x), ctypes.byref(cw), _ptr(dy), ctypes.c_float(d_aux),
-                            ctypes.byref(co), _ptr(gu), ws.ptr, ctypes.byref(cg), bws.ptr, _stream(stream)),
-           "moe_backward")
+    _check(_run([x, dy, gu, ws.buf, bws.buf, *weights.tensors(), *outputs.tensors(), *grads.tensors()], stream,
+                lib.moe_backward, ctypes.byref(cfg), _ptr(x), ctypes.byref(cw), _ptr(dy), ctypes.c_float(d_aux),
+                ctypes.byref(co), _ptr(gu), ws.ptr, ctypes.byref(cg), bws.ptr), "moe_backward")
     return grads
 
 
@@ -488,8 +530,14 @@ def moe_dispatch_noalloc(cfg: MoEConfig, x, topk_idx, *, counts=None, offsets=No
     slot_of = slot_of if slot_of is not None else torch.empty((Tu, K), dtype=torch.int32, device=dev)
     row_token = row_token if row_token is not None else torch.empty((Tu * K,), dtype=torch.int32, device=dev)
     x_packed = x_packed if x_packed is not None else torch.empty((Tu * K, hu), dtype=dt, device=dev)
-    code = lib.moe_dispatch_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts), _ptr(offsets),
-                                    _ptr(slot_of), _ptr(row_token), _ptr(x_packed), _stream(stream))
+    _req(counts, "counts", (E,), torch.int32)
+    _req(offsets, "offsets", (E + 1,), torch.int32)
+    _req(slot_of, "slot_of", (Tu, K), torch.int32)
+    _req(row_token, "row_token", (Tu * K,), torch.int32)
+    _req(x_packed, "x_packed", (Tu * K, hu), dt)
+    code = _run([x, topk_idx, counts, offsets, slot_of, row_token, x_packed], stream, lib.moe_dispatch_noalloc,
+                ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts), _ptr(offsets), _ptr(slot_of),
+                _ptr(row_token), _ptr(x_packed))
     if code == MOE_ERR_UNSUPPORTED:
         raise MoEError(code, f"moe_dispatch_noalloc: {Tu} units x {E} experts need more than the "
                              f"{NOALLOC_SCRATCH_BYTES} bytes of fixed scratch")

@@ -13,7 +13,7 @@ no blocking, fusion or reordering beyond the definitions below. Sources, by page
               communication volume 2·Tokens·K·h·sizeof(dtype)),
           §4 (aux loss L_aux = α·E·Σ f_i·P_i; capacity C = CF·K·T/E, overflow tokens dropped),
           §5 (node-limited routing: a token's K experts lie in at most M node groups),
-          worked example and exercise solutions (expert→rank map, per-rank load, imbalance).
+          worked example (expert→rank placement, per-rank load, imbalance, utilisation).
   [HAI]   "HAI-LLM MoE：一键实现大模型的混合专家并行训练", §"HAI-LLM 上的使用" (alpha=0.01, top_k).
   [CH10]  "Chương 10: Song song MoE", §4 (aux-loss-free balancing by a per-expert bias).
   [MHL]   "Multi-Head LatentMoE 与 Head 并行", §摘要 and 评论 §1 (input split into heads, each
@@ -374,38 +374,38 @@ def forward(x: np.ndarray, w_g: np.ndarray, experts: ExpertProvider, *, E: int, 
 
 
 # ---------------------------------------------------------------------------------------------
-# [Lesson 10 worked example and exercise] load reporting
+# [Lesson 10 worked example] load reporting of an expert-parallel placement
 
 
-def expert_to_rank(num_experts: int, experts_per_rank: int) -> dict:
-    """Rank r holds experts [r·epr, (r+1)·epr).  [Lesson 10 exercise]"""
-    return {e: e // experts_per_rank for e in range(num_experts)}
+def expert_to_rank(num_experts: int, experts_per_rank: int) -> np.ndarray:
+    """Owning rank of every expert [E] when each rank holds a contiguous block of experts_per_rank
+    experts (expert e lives on rank ⌊e / experts_per_rank⌋).  [Lesson 10 §3, worked example]"""
+    return np.arange(num_experts, dtype=np.int64) // int(experts_per_rank)
 
 
 def load_per_rank(tokens_per_expert, experts_per_rank: int) -> list:
-    """Per-rank load = tokens received by the rank's experts.  [Lesson 10 exercise]"""
-    n = len(tokens_per_expert)
-    loads = [0] * (n // experts_per_rank)
-    m = expert_to_rank(n, experts_per_rank)
-    for e, c in enumerate(tokens_per_expert):
-        loads[m[e]] += int(c)
-    return loads
+    """Tokens each rank's experts receive: the per-expert loads summed over each rank's block.
+    [Lesson 10 worked example]"""
+    c = np.asarray(tokens_per_expert, dtype=np.int64)
+    owner = expert_to_rank(c.size, experts_per_rank)
+    return np.bincount(owner, weights=c, minlength=c.size // int(experts_per_rank)).astype(np.int64).tolist()
 
 
 def imbalance(loads) -> float:
-    """max load / mean load.  [Lesson 10 worked example]"""
-    loads = list(loads)
-    if not loads or sum(loads) == 0:
-        raise ValueError("loads must be non-empty with a positive total")
-    return max(loads) / (sum(loads) / len(loads))
+    """Peak-to-mean ratio of the rank loads.  [Lesson 10 worked example]"""
+    a = np.asarray(loads, dtype=np.float64)
+    if a.size == 0 or not a.sum() > 0:
+        raise ValueError("imbalance needs at least one rank and some load")
+    return float(a.max() / a.mean())
 
 
 def routing_volume(tokens_per_expert) -> int:
-    """Routed tokens of one forward (upper bound of the all-to-all volume in tokens).  [Lesson 10 exercise]"""
-    return int(sum(tokens_per_expert))
+    """Token copies one step routes (each (token, pick) is one copy): the sum of the per-expert
+    loads, the token count of the dispatch traffic.  [Lesson 10 §3]"""
+    return int(np.asarray(tokens_per_expert, dtype=np.int64).sum())
 
 
 def utilisation(loads) -> float:
     """Σ load / (ranks · max load): useful share of the step when the slowest rank sets it.  [Lesson 10 worked example]"""
-    loads = list(loads)
-    return sum(loads) / (len(loads) * max(loads))
+    a = np.asarray(loads, dtype=np.float64)
+    return float(a.sum() / (a.size * a.max()))

@@ -1,5 +1,5 @@
 """Shared helpers of the parity tests: seeded workloads on the device and for the oracle, the
-tolerances, and the near-tie analysis of routing decisions made on differently rounded logits."""
+tolerances, and the bit-exact routing check on the GPU's own fp32 logits."""
 from __future__ import annotations
 
 import math
@@ -112,42 +112,29 @@ def tol_ok(got: np.ndarray, ref: np.ndarray, dtype: str):
     return err <= bound, err, bound
 
 
-def routing_margins(keys: np.ndarray, idx: np.ndarray, n_groups: int, topk_groups: int) -> np.ndarray:
-    """Per unit, the smallest gap between a decision's winner and loser in the oracle's keys:
-    the K-th vs (K+1)-th eligible key, and (group limit) the last kept vs first dropped group score."""
-    T, E = keys.shape
-    K = idx.shape[1]
-    elig = O.group_limit(keys, n_groups, topk_groups)
-    kk = np.where(elig, keys, -np.inf)
-    srt = -np.sort(-kk, axis=1)
-    m = srt[:, K - 1] - (srt[:, K] if K < E else -np.inf)
-    if n_groups > 1:
-        gs = E // n_groups
-        top = -np.sort(-keys.reshape(T, n_groups, gs), axis=2)
-        score = top[:, :, 0] + (top[:, :, 1] if gs > 1 else 0)
-        gsrt = -np.sort(-score, axis=1)
-        gm = gsrt[:, topk_groups - 1] - (gsrt[:, topk_groups] if topk_groups < n_groups else -np.inf)
-        m = np.minimum(m, gm)
-    return m
+def route_on_gpu_logits(inp: "Inputs", outs, exact_logits: Optional[np.ndarray] = None):
+    """The routing check of a forward, bit for bit.
 
+    1. The GPU's fp32 logits (logit bias included) lie within the rigorous fp32 error bound of the
+       exact float64 logits.
+    2. The oracle routes on those same fp32 logits: its picks must equal the GPU's for every unit
+       (softmax keys are the logits themselves; sigmoid keys σ(l) + b are formed in float64 on
+       both sides).
 
-def check_routing(gpu_idx: np.ndarray, ref_idx: np.ndarray, keys: np.ndarray, key_err: np.ndarray,
-                  shape: MoEShape):
-    """Exact where the oracle's decision margin exceeds twice the key error (per unit, twice for
-    group scores); elsewhere the GPU's picks must be a valid near-optimal choice.
-    Returns (n_ambiguous, n_differ)."""
-    E, K = shape.E, shape.K
-    margin = routing_margins(keys, ref_idx, shape.n_groups, shape.topk_groups)
-    slack = 4.0 * key_err.max(axis=1)
-    amb = margin <= slack
-    same = (gpu_idx == ref_idx).all(axis=1)
-    bad_robust = np.nonzero(~amb & ~same)[0]
-    assert bad_robust.size == 0, f"routing differs on units with a clear margin: {bad_robust[:10]}"
-    n_differ = int((~same).sum())
-    for u in np.nonzero(~same)[0]:
-        g = gpu_idx[u]
-        assert len(set(g.tolist())) == K and g.min() >= 0 and g.max() < E
-        if shape.n_groups > 1:
-            assert len({int(e) // (E // shape.n_groups) for e in g}) <= shape.topk_groups
-        assert keys[u, g].sum() >= keys[u, ref_idx[u]].sum() - 2 * K * slack[u]
-    return int(amb.sum()), n_differ
+    Returns (gpu picks [T'][K] int64, oracle gates at those logits, the GPU logits as float64).
+    """
+    s = inp.shape
+    gl = as_f64(outs.logits)
+    if exact_logits is None:
+        b = inp.bf16
+        exact_logits = O.router_logits(O.split_heads(widen(inp.x, b), s.n_heads), widen(inp.w_g, b),
+                                       inp.logit_bias)
+    bound = inp.logit_error_bound()
+    over = np.abs(gl - exact_logits) - bound
+    assert (over <= 0).all(), f"GPU logits outside the fp32 error bound by {float(over.max()):.3e}"
+    idx, gate, _ = O.route(gl, s.score, s.K, inp.select_bias, s.n_groups, s.topk_groups)
+    gidx = bits_of(outs.topk_idx).astype(np.int64)
+    bad = np.nonzero((gidx != idx).any(axis=1))[0]
+    assert bad.size == 0, (f"{bad.size} of {s.T_units} units routed differently from the oracle on the same "
+                           f"fp32 logits, e.g. unit {bad[0]}: GPU {gidx[bad[0]].tolist()} oracle {idx[bad[0]].tolist()}")
+    return gidx, gate, gl

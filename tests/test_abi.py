@@ -34,6 +34,22 @@ def test_library_exports_every_declared_symbol():
     assert lib.moe_abi_version() == 2
 
 
+_KEEP = []
+
+
+def _addr(nbytes: int = 1 << 20, offset: int = 0) -> int:
+    """An address for the host-side rejection tests below, which must fail before the library
+    enqueues anything. With a GPU present it is real device memory of nbytes (each test sizes it
+    to what the rejected call would touch), so even a check that wrongly let a call through would
+    stay inside valid memory; without one no kernel can be launched at all, and a fixed,
+    256-byte-aligned number stands in."""
+    if torch.cuda.is_available():
+        t = torch.zeros(nbytes + 256, dtype=torch.uint8, device="cuda")
+        _KEEP.append(t)
+        return t.data_ptr() + offset
+    return 4096 + offset
+
+
 def _cfg(**kw):
     base = dict(T=256, h=128, E=8, K=2, d_ff=256, capacity_factor=1.25, dtype="f32")
     base.update(kw)
@@ -73,9 +89,10 @@ def test_missing_workspace_and_pointers_rejected():
     lib = M.load_library()
     cfg = _cfg()
     w = M.MoEWeights()
-    assert lib.moe_forward(ctypes.byref(cfg), 16, ctypes.byref(w), 16, None, None, None) == M.MOE_ERR_WORKSPACE
-    assert lib.moe_forward(ctypes.byref(cfg), 16, ctypes.byref(w), 16, None, 4096, None) == M.MOE_ERR_INVALID_ARG
-    assert lib.moe_route(ctypes.byref(cfg), None, None, None, None, None, None, None, None, 4096, None) \
+    x, y, ws = _addr(), _addr(), _addr(M.workspace_size(cfg))
+    assert lib.moe_forward(ctypes.byref(cfg), x, ctypes.byref(w), y, None, None, None) == M.MOE_ERR_WORKSPACE
+    assert lib.moe_forward(ctypes.byref(cfg), x, ctypes.byref(w), y, None, ws, None) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(ctypes.byref(cfg), None, None, None, None, None, None, None, None, ws, None) \
         == M.MOE_ERR_INVALID_ARG
     assert lib.moe_get_status(None, None) == M.MOE_ERR_WORKSPACE
     assert M.status_string(M.MOE_ERR_TIMEOUT) == "kernel wait timed out"
@@ -95,9 +112,10 @@ def test_backward_sizes_and_support_on_host():
     for bad in (_cfg(), _cfg(dtype="bf16", h=96, d_ff=128), _cfg(dtype="bf16", h=128, d_ff=96)):
         assert lib.moe_backward_workspace_size(ctypes.byref(bad)) == 0  # fp32, or h' / d_ff not multiples of 64
         g = M.MoEGrads()
-        assert lib.moe_backward(ctypes.byref(bad), None, None, None, ctypes.c_float(1.0), None, None, 4096,
-                                ctypes.byref(g), 4096, None) == M.MOE_ERR_UNSUPPORTED
-        assert lib.moe_forward_train(ctypes.byref(bad), None, None, None, None, None, 4096, None) \
+        ws = _addr(M.workspace_size(bad))
+        assert lib.moe_backward(ctypes.byref(bad), None, None, None, ctypes.c_float(1.0), None, None, ws,
+                                ctypes.byref(g), ws, None) == M.MOE_ERR_UNSUPPORTED
+        assert lib.moe_forward_train(ctypes.byref(bad), None, None, None, None, None, ws, None) \
             == M.MOE_ERR_UNSUPPORTED
 
 
@@ -105,13 +123,16 @@ def test_backward_rejects_missing_buffers_on_host():
     lib = M.load_library()
     cfg = _cfg(dtype="bf16")
     w, o, g = M.MoEWeights(), M.MoEOutputs(), M.MoEGrads()
-    args = lambda ws, bws: (ctypes.byref(cfg), 16, ctypes.byref(w), 16, ctypes.c_float(1.0), ctypes.byref(o), 16,
+    x, dy, gu = _addr(), _addr(), _addr(M.saved_gu_size(cfg))
+    ws = _addr(M.workspace_size(cfg))
+    bws = _addr(lib.moe_backward_workspace_size(ctypes.byref(cfg)))
+    args = lambda ws, bws: (ctypes.byref(cfg), x, ctypes.byref(w), dy, ctypes.c_float(1.0), ctypes.byref(o), gu,
                             ws, ctypes.byref(g), bws, None)
-    assert lib.moe_backward(*args(None, 4096)) == M.MOE_ERR_WORKSPACE
-    assert lib.moe_backward(*args(4096, 4100)) == M.MOE_ERR_WORKSPACE   # misaligned backward scratch
-    assert lib.moe_backward(*args(4096, 4096)) == M.MOE_ERR_INVALID_ARG  # no weights / saved outputs
+    assert lib.moe_backward(*args(None, bws)) == M.MOE_ERR_WORKSPACE
+    assert lib.moe_backward(*args(ws, bws + 4)) == M.MOE_ERR_WORKSPACE   # misaligned backward scratch
+    assert lib.moe_backward(*args(ws, bws)) == M.MOE_ERR_INVALID_ARG     # no weights / saved outputs
     # the training forward needs the saved outputs
-    assert lib.moe_forward_train(ctypes.byref(cfg), 16, ctypes.byref(w), 16, None, 16, 4096, None) \
+    assert lib.moe_forward_train(ctypes.byref(cfg), x, ctypes.byref(w), dy, None, gu, ws, None) \
         == M.MOE_ERR_INVALID_ARG
 
 

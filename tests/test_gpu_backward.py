@@ -1,8 +1,8 @@
 """Parity of moe_forward_train + moe_backward against the backward oracle (GPU).
 
-The GPU's routing is first checked against the oracle (exact where the decision margin exceeds
-the logit error bound, valid elsewhere); the oracle's gradient is then taken at the GPU's picks,
-which is what the backward differentiates (routing held fixed).
+The GPU's routing is first checked bit for bit against the oracle's routing of the GPU's own fp32
+logits; the oracle's gradient is then taken at the GPU's picks, which is what the backward
+differentiates (routing held fixed).
 
 Tolerance, from the rounding points of the bf16 path: dY_packed, dG|dU, dX_packed, G|U and H are
 each rounded to bf16 once (unit roundoff u = 2^-8 relative per element), and every gradient is a
@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle.moe_backward as B
-from harness import Inputs, as_f64, bits_of, check_routing, config_of, to_device, widen
+from harness import Inputs, as_f64, bits_of, config_of, route_on_gpu_logits, to_device, widen
 from mixture_experts_layer_96_b300 import (BackwardWorkspace, ForwardOutputs, Workspace, moe_backward,
                                            moe_forward, moe_forward_train)
 from workloads import WORKLOADS, Generator, MoEShape, scaled
@@ -68,12 +68,9 @@ def run_train(inp: Inputs):
 
 
 def gpu_picks_checked(inp: Inputs, outs):
-    s = inp.shape
-    ref = inp.oracle_forward()
-    bound = inp.logit_error_bound()
-    gidx = bits_of(outs.topk_idx).astype(np.int64)
-    key_err = bound if s.score == "softmax" else bound / 4.0
-    check_routing(gidx, ref.idx, ref.keys, key_err, s)
+    """The GPU's picks, after checking them bit for bit against the oracle's routing of the same
+    fp32 logits."""
+    gidx, _, _ = route_on_gpu_logits(inp, outs)
     return gidx
 
 
@@ -200,10 +197,7 @@ def test_backward_parity_full_size_sampled(name):
     inp = Inputs.make(shape)
     cfg, x, lw, ws, outs, y, gu, dy, bws, g = run_train(inp)
     ref = inp.oracle_forward(sample_units=np.array([0]))   # routing of all units; y of one
-    bound = inp.logit_error_bound()
-    gidx = bits_of(outs.topk_idx).astype(np.int64)
-    key_err = bound if shape.score == "softmax" else bound / 4.0
-    check_routing(gidx, ref.idx, ref.keys, key_err, shape)
+    gidx, _, _ = route_on_gpu_logits(inp, outs, exact_logits=ref.logits)
     counts = np.bincount(gidx.reshape(-1), minlength=shape.E)
     slot = bits_of(outs.slot_of)
     rng = np.random.default_rng(321)

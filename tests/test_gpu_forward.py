@@ -1,16 +1,18 @@
 """End-to-end parity of moe_forward against the oracle (GPU).
 
-The oracle routes on its own float64 logits. Where a unit's routing decision has a margin larger
-than the fp32 logits' error bound, the GPU must pick exactly the oracle's experts; inside the
-bound either choice is valid and is checked for validity. Given the (checked) routing, counts,
-offsets and packed slots must match the oracle bit-exactly, and y must meet the layer's float
-tolerance.
+Routing is checked bit for bit: the GPU's fp32 router logits (written by moe_forward, logit bias
+included) must lie within the fp32 error bound of the exact logits, and the oracle, routing on
+those same fp32 logits, must pick exactly the GPU's experts for every unit. Counts, offsets and
+packed slots must then equal the oracle's dispatch of those picks, the gates the oracle's gates
+on those logits, and y must meet the layer's float tolerance against the oracle's float64 layer
+at those picks.
 """
 import numpy as np
 import pytest
 import torch
 
-from harness import Inputs, as_f64, bits_of, check_routing, config_of, tol_ok
+import oracle.moe_oracle as O
+from harness import Inputs, as_f64, bits_of, config_of, route_on_gpu_logits, tol_ok
 from mixture_experts_layer_96_b300 import (ForwardOutputs, Workspace, moe_combine, moe_dispatch,
                                            moe_expert_ffn, moe_forward, moe_route)
 from workloads import WORKLOADS, MoEShape, scaled
@@ -50,24 +52,23 @@ def run_forward(inp: Inputs):
 
 
 def check_forward(inp: Inputs, y, outs, sample=None):
+    """`sample`: None (every unit), an array of units, or a callable that picks the units from
+    the oracle's dispatch of the GPU's picks."""
     s = inp.shape
-    ref = inp.oracle_forward(sample_units=sample)
-    bound = inp.logit_error_bound()
-    gl = as_f64(outs.logits)
-    assert (np.abs(gl - ref.logits) <= bound).all(), float(np.max(np.abs(gl - ref.logits) - bound))
-    gidx = bits_of(outs.topk_idx).astype(np.int64)
-    key_err = bound if s.score == "softmax" else bound / 4.0  # σ is 1/4-Lipschitz
-    n_amb, n_diff = check_routing(gidx, ref.idx, ref.keys, key_err, s)
-    if n_diff:
-        ref = inp.oracle_forward(sample_units=sample, idx_override=gidx)
+    gidx, gate_ref, gl = route_on_gpu_logits(inp, outs)
+    if callable(sample):
+        sample = sample(O.dispatch(gidx, s.E, O.capacity(s.capacity_factor, s.K, s.T_units, s.E)))
+    # the oracle's layer at the GPU's picks (float64 logits, gates and experts)
+    ref = inp.oracle_forward(sample_units=sample, idx_override=gidx)
     d = ref.dispatch
     np.testing.assert_array_equal(bits_of(outs.counts), d.counts)
     np.testing.assert_array_equal(bits_of(outs.offsets), d.offsets)
     np.testing.assert_array_equal(bits_of(outs.slot_of), d.slot_of)
-    gate_tol = 2.0 * float(bound.max()) + 2e-6
-    np.testing.assert_allclose(as_f64(outs.topk_gate), ref.gate, atol=gate_tol, rtol=0)
+    # gates from the same fp32 logits: fp32 softmax / sigmoid normalisation against float64
+    np.testing.assert_allclose(as_f64(outs.topk_gate), gate_ref, atol=2e-6, rtol=0)
+    aux_ref = O.aux_loss(gl, gidx, s.E, s.K, s.aux_alpha, s.score)
     aux = float(outs.aux.item())
-    assert abs(aux - ref.aux) <= 1e-4 * abs(ref.aux) + 1e-7, (aux, ref.aux)
+    assert abs(aux - aux_ref) <= 1e-4 * abs(aux_ref) + 1e-7, (aux, aux_ref)
     yg = as_f64(y)
     if sample is None:
         ok, err, tb = tol_ok(yg, ref.y, s.dtype)
@@ -77,7 +78,7 @@ def check_forward(inp: Inputs, y, outs, sample=None):
         want = np.stack([ref.y_units[int(u)] for u in sample])
         ok, err, tb = tol_ok(got, want, s.dtype)
     assert ok, f"max |y - y_ref| = {err} > {tb}"
-    return n_amb, n_diff
+    return gidx
 
 
 @pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
@@ -148,13 +149,29 @@ def test_forward_empty_batch():
 FULL = ["mixtral_bf16", "skewed_bf16", "multihead_bf16", "tiny_f32", "finegrained_bf16"]
 
 
+def tile_covering_sample(n_min: int, seed: int = 123):
+    """Units whose outputs the full-size check computes: for every expert with rows, the units
+    of its first and last packed row (so each expert's first and last m-tile is looked at,
+    ragged tails included), plus random units up to n_min."""
+    def pick(d):
+        units = set()
+        for e in range(len(d.offsets) - 1):
+            r0, r1 = int(d.offsets[e]), int(d.offsets[e + 1])
+            if r1 > r0:
+                units.add(int(d.row_token[r0]))
+                units.add(int(d.row_token[r1 - 1]))
+        rng = np.random.default_rng(seed)
+        T = d.slot_of.shape[0]
+        while len(units) < min(n_min, T):
+            units.add(int(rng.integers(T)))
+        return np.array(sorted(units), dtype=np.int64)
+    return pick
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", FULL)
 def test_forward_parity_full_size_sampled(name):
     shape = WORKLOADS[name]
     inp = Inputs.make(shape)
     y, outs = run_forward(inp)
-    rng = np.random.default_rng(123)
-    n = 8 if shape.E >= 256 else 16
-    sample = np.sort(rng.choice(shape.T_units, size=min(n, shape.T_units), replace=False))
-    check_forward(inp, y, outs, sample=sample)
+    check_forward(inp, y, outs, sample=tile_covering_sample(256))

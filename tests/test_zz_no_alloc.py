@@ -55,10 +55,26 @@ def test_noalloc_dispatch_equals_dispatch_on_two_calls_in_a_row():
 
 
 def test_noalloc_dispatch_rejects_problems_past_its_scratch():
-    cfg = M.make_config(200_000, 64, 256, 8, 64)  # 782 chunks x 256 experts x 8 B > 1 MiB
+    """A problem whose scratch does not fit the fixed array is refused before anything is enqueued.
+    Every buffer passed is real device memory of the full size the call would use, so even a call
+    that wrongly went ahead would stay inside its buffers."""
+    T, h, E, K = 200_000, 64, 256, 8   # 1563 chunks x 256 experts x 8 B > 1 MiB
+    cfg = M.make_config(T, h, E, K, 64)
+    dev = "cuda"
+    x = torch.zeros((T, h), dtype=torch.bfloat16, device=dev)
+    idx = torch.zeros((T, K), dtype=torch.int32, device=dev)
+    counts = torch.empty((E,), dtype=torch.int32, device=dev)
+    offsets = torch.empty((E + 1,), dtype=torch.int32, device=dev)
+    slot_of = torch.empty((T, K), dtype=torch.int32, device=dev)
+    row_token = torch.empty((T * K,), dtype=torch.int32, device=dev)
+    x_packed = torch.empty((T * K, h), dtype=torch.bfloat16, device=dev)
     lib = M.load_library()
-    code = lib.moe_dispatch_noalloc(ctypes.byref(cfg), 16, 16, None, 16, 16, 16, 16, None)
+    before = M.launch_count()
+    code = lib.moe_dispatch_noalloc(ctypes.byref(cfg), x.data_ptr(), idx.data_ptr(), counts.data_ptr(),
+                                    offsets.data_ptr(), slot_of.data_ptr(), row_token.data_ptr(),
+                                    x_packed.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert code == M.MOE_ERR_UNSUPPORTED
+    assert M.launch_count() == before   # nothing was launched
     with pytest.raises(M.MoEError, match="fixed scratch"):
-        M.moe_dispatch_noalloc(cfg, torch.zeros((200_000, 64), dtype=torch.bfloat16, device="cuda"),
-                               torch.zeros((200_000, 8), dtype=torch.int32, device="cuda"))
+        M.moe_dispatch_noalloc(cfg, x, idx, counts=counts, offsets=offsets, slot_of=slot_of, row_token=row_token,
+                               x_packed=x_packed)
