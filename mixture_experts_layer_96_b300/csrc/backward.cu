@@ -212,7 +212,30 @@ __global__ void bwd_dx_kernel(const uint4* __restrict__ dx_packed, const int32_t
   }
 }
 
+// W_gᵀ[n][k] = W_g[k][n] (32 x 32 tiles through shared memory).
+__global__ void __launch_bounds__(256)
+router_transpose_kernel(const __nv_bfloat16* __restrict__ w, int hu, int E, __nv_bfloat16* __restrict__ wt) {
+  __shared__ __nv_bfloat16 tile[32][33];
+  const int k0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int r = ty; r < 32; r += 8) {
+    const int k = k0 + r, n = n0 + tx;
+    tile[r][tx] = (k < hu && n < E) ? w[(int64_t)k * E + n] : __float2bfloat16(0.f);
+  }
+  __syncthreads();
+  for (int r = ty; r < 32; r += 8) {
+    const int n = n0 + r, k = k0 + tx;
+    if (n < E && k < hu) wt[(int64_t)n * hu + k] = tile[tx][r];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_router_transpose(const Problem& p, const void* w_router, void* wt, cudaStream_t s) {
+  if (p.Tu == 0) return cudaSuccess;
+  return launch_kernel(router_transpose_kernel, dim3((p.hu + 31) / 32, (p.E + 31) / 32), dim3(256), 0, s, 1, false,
+                       static_cast<const __nv_bfloat16*>(w_router), p.hu, p.E, static_cast<__nv_bfloat16*>(wt));
+}
 
 cudaError_t launch_backward_misc_combine(const Problem& p, const void* dy, const void* y_packed,
                                          const int32_t* slot_of, const float* gate, void* dy_packed,

@@ -23,6 +23,8 @@ combine_kernel(const T* __restrict__ y_packed, const int32_t* __restrict__ slot_
   const uint32_t lane = threadIdx.x & 31u;
   const uint4* yp = reinterpret_cast<const uint4*>(y_packed);
   uint4* yo = reinterpret_cast<uint4*>(y);
+  griddep_launch_dependents();
+  griddep_wait();
   for (uint64_t wb = ((uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 64u; wb < total;
        wb += nwarps * 64u) {
     uint4 raw[2][KMAX];
@@ -89,6 +91,8 @@ combine_scalar_kernel(const T* __restrict__ y_packed, const int32_t* __restrict_
                       int64_t rows, uint32_t* status) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  griddep_launch_dependents();
+  griddep_wait();
   for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < Tu; u += warps) {
     for (int c = lane; c < hu; c += 32) {
       float acc = 0.f;
@@ -104,7 +108,7 @@ combine_scalar_kernel(const T* __restrict__ y_packed, const int32_t* __restrict_
 }
 
 cudaError_t launch_combine(const Problem& p, const void* y_packed, const int32_t* slot_of,
-                           const float* gate, void* y, uint32_t* status, cudaStream_t s) {
+                           const float* gate, void* y, uint32_t* status, cudaStream_t s, bool pdl) {
   if (p.Tu == 0) return cudaSuccess;
   const int sms = device_sm_count();
   int64_t blocks = (p.Tu * ((int64_t)p.hu * (int64_t)p.elt / 16) + 511) / 512;
@@ -113,25 +117,22 @@ cudaError_t launch_combine(const Problem& p, const void* y_packed, const int32_t
   const bool vec = ((int64_t)p.hu * (int64_t)p.elt) % 16 == 0 &&
                    (reinterpret_cast<uintptr_t>(y_packed) & 15) == 0 &&
                    (reinterpret_cast<uintptr_t>(y) & 15) == 0;
-  const unsigned b = (unsigned)blocks;
+  const dim3 g((unsigned)blocks), b(256);
   const int kb = p.K <= 2 ? 2 : (p.K <= 4 ? 4 : 8);
   if (p.bf16) {
     auto yp = static_cast<const __nv_bfloat16*>(y_packed);
     auto yo = static_cast<__nv_bfloat16*>(y);
-    if (!vec) combine_scalar_kernel<__nv_bfloat16><<<b, 256, 0, s>>>(yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
-    else if (kb == 2) combine_kernel<__nv_bfloat16, 2><<<b, 256, 0, s>>>(yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
-    else if (kb == 4) combine_kernel<__nv_bfloat16, 4><<<b, 256, 0, s>>>(yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
-    else combine_kernel<__nv_bfloat16, 8><<<b, 256, 0, s>>>(yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
-  } else {
-    auto yp = static_cast<const float*>(y_packed);
-    auto yo = static_cast<float*>(y);
-    if (!vec) combine_scalar_kernel<float><<<b, 256, 0, s>>>(yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
-    else if (kb == 2) combine_kernel<float, 2><<<b, 256, 0, s>>>(yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
-    else if (kb == 4) combine_kernel<float, 4><<<b, 256, 0, s>>>(yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
-    else combine_kernel<float, 8><<<b, 256, 0, s>>>(yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
+    if (!vec) return launch_kernel(combine_scalar_kernel<__nv_bfloat16>, g, b, 0, s, 1, pdl, yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
+    if (kb == 2) return launch_kernel(combine_kernel<__nv_bfloat16, 2>, g, b, 0, s, 1, pdl, yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
+    if (kb == 4) return launch_kernel(combine_kernel<__nv_bfloat16, 4>, g, b, 0, s, 1, pdl, yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
+    return launch_kernel(combine_kernel<__nv_bfloat16, 8>, g, b, 0, s, 1, pdl, yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
   }
-  note_launch();
-  return cudaGetLastError();
+  auto yp = static_cast<const float*>(y_packed);
+  auto yo = static_cast<float*>(y);
+  if (!vec) return launch_kernel(combine_scalar_kernel<float>, g, b, 0, s, 1, pdl, yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
+  if (kb == 2) return launch_kernel(combine_kernel<float, 2>, g, b, 0, s, 1, pdl, yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
+  if (kb == 4) return launch_kernel(combine_kernel<float, 4>, g, b, 0, s, 1, pdl, yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
+  return launch_kernel(combine_kernel<float, 8>, g, b, 0, s, 1, pdl, yp, slot_of, gate, yo, p.Tu, p.K, p.hu, p.rows, status);
 }
 
 }  // namespace moe

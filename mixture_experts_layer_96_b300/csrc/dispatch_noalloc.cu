@@ -16,25 +16,6 @@
 
 namespace moe {
 
-// Kernels of the regular dispatch (dispatch.cu), launched here on the static scratch.
-__global__ void dispatch_hist_kernel(const int32_t* __restrict__ idx, int64_t Tu, int K, int E,
-                                     int32_t* __restrict__ chunk_hist, uint32_t* status);
-__global__ void dispatch_scan_kernel(const int32_t* __restrict__ chunk_hist, int64_t nchunks, int E,
-                                     int64_t C, int32_t* __restrict__ chunk_base,
-                                     int32_t* __restrict__ counts_ws, int32_t* __restrict__ offsets_ws,
-                                     int32_t* counts_out, int32_t* offsets_out, unsigned int* ticket);
-__global__ void dispatch_rank_kernel(const int32_t* __restrict__ idx, int64_t Tu, int K, int E, int64_t C,
-                                     const int32_t* __restrict__ chunk_base,
-                                     const int32_t* __restrict__ offsets, int32_t* __restrict__ slot_of,
-                                     int32_t* __restrict__ row_token, int64_t rows);
-__global__ void dispatch_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row_token,
-                                       const int32_t* __restrict__ offsets, int E, int64_t row_vecs,
-                                       uint4* __restrict__ x_packed);
-__global__ void dispatch_gather_scalar_kernel(const unsigned char* __restrict__ x,
-                                              const int32_t* __restrict__ row_token,
-                                              const int32_t* __restrict__ offsets, int E,
-                                              int64_t row_bytes, unsigned char* __restrict__ x_packed);
-
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB per device
 constexpr int kNoAllocMaxDevices = 64;
 
@@ -88,41 +69,15 @@ extern "C" MOE_API moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, co
   void* base = nullptr;
   if (scratch_address(&base) != cudaSuccess) return MOE_ERR_CUDA;
   char* sc = static_cast<char*>(base);
-  unsigned int* ticket = reinterpret_cast<unsigned int*>(sc + off_ticket);
-  int32_t* counts_ws = reinterpret_cast<int32_t*>(sc + off_counts);
-  int32_t* offsets_ws = reinterpret_cast<int32_t*>(sc + off_offsets);
-  int32_t* chunk_hist = reinterpret_cast<int32_t*>(sc + off_hist);
-  int32_t* chunk_base = reinterpret_cast<int32_t*>(sc + off_base);
-  const cudaStream_t s = (cudaStream_t)stream;
-
-  const unsigned nch = (unsigned)(p.nchunks > 0 ? p.nchunks : 0);
-  if (nch > 0) {
-    dispatch_hist_kernel<<<nch, kChunk, 0, s>>>(topk_idx, p.Tu, p.K, p.E, chunk_hist, nullptr);
-    note_launch();
-  }
-  dispatch_scan_kernel<<<p.E, 256, 0, s>>>(chunk_hist, p.nchunks, p.E, p.C, chunk_base, counts_ws,
-                                          offsets_ws, counts, offsets, ticket);
-  note_launch();
-  dispatch_rank_kernel<<<nch > 0 ? nch : 1, kChunk, 0, s>>>(topk_idx, p.Tu, p.K, p.E, p.C, chunk_base,
-                                                           offsets_ws, slot_of, row_token, p.rows);
-  note_launch();
-  if (p.rows > 0) {
-    const int64_t row_bytes = (int64_t)p.hu * (int64_t)p.elt;
-    int64_t blocks = (p.rows * (row_bytes / 16) + 1023) / 1024;
-    const int64_t cap = (int64_t)device_sm_count() * 8;
-    if (blocks < 1) blocks = 1;
-    if (blocks > cap) blocks = cap;
-    if (row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
-        (reinterpret_cast<uintptr_t>(x_packed) & 15) == 0) {
-      dispatch_gather_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4*>(x), row_token,
-                                                             offsets_ws, p.E, row_bytes / 16,
-                                                             static_cast<uint4*>(x_packed));
-    } else {
-      dispatch_gather_scalar_kernel<<<(unsigned)blocks, 256, 0, s>>>(
-          static_cast<const unsigned char*>(x), row_token, offsets_ws, p.E, row_bytes,
-          static_cast<unsigned char*>(x_packed));
-    }
-    note_launch();
-  }
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  DispatchScratch d;
+  d.ticket = reinterpret_cast<unsigned int*>(sc + off_ticket);
+  d.counts = reinterpret_cast<int32_t*>(sc + off_counts);
+  d.offsets = reinterpret_cast<int32_t*>(sc + off_offsets);
+  d.chunk_hist = reinterpret_cast<int32_t*>(sc + off_hist);
+  d.chunk_base = reinterpret_cast<int32_t*>(sc + off_base);
+  d.status = nullptr;  // no workspace, so no status word: bad picks only get slot -1
+  return launch_dispatch_from_idx(p, x, topk_idx, counts, offsets, slot_of, row_token, x_packed, d,
+                                  (cudaStream_t)stream) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
 }

@@ -22,6 +22,8 @@ expert_gemm_simt_kernel(const float* __restrict__ A, const float* __restrict__ B
   __shared__ float Bs0[kSK][kSB + 4];
   __shared__ float Bs1[SWIGLU ? kSK : 1][kSB + 4];
   const int tid = threadIdx.x;
+  griddep_launch_dependents();
+  griddep_wait();
   if (tid < 32) {
     const bool ok = warp_tile_prefix(offsets, E, kSB, rows_cap, s_off, s_pre);
     if (tid == 0) {
@@ -88,25 +90,22 @@ expert_gemm_simt_kernel(const float* __restrict__ A, const float* __restrict__ B
 
 cudaError_t launch_expert_ffn_simt(const Problem& p, const void* x_packed, const int32_t* offsets,
                                    const void* w_gate, const void* w_up, const void* w_down,
-                                   void* hidden, void* y_packed, uint32_t* status, cudaStream_t s) {
+                                   void* hidden, void* y_packed, uint32_t* status, cudaStream_t s, bool pdl) {
   if (p.rows == 0) return cudaSuccess;
   const int64_t max_m = (p.rows + kSB - 1) / kSB + p.E;
   const int nt1 = (p.d_ff + kSB - 1) / kSB, nt2 = (p.hu + kSB - 1) / kSB;
   const int cap = device_sm_count() * 8;
   int g1 = (int)((max_m * nt1 < cap) ? max_m * nt1 : cap);
   int g2 = (int)((max_m * nt2 < cap) ? max_m * nt2 : cap);
-  expert_gemm_simt_kernel<true><<<g1, 256, 0, s>>>(
-      static_cast<const float*>(x_packed), static_cast<const float*>(w_gate),
-      static_cast<const float*>(w_up), offsets, p.E, p.hu, p.d_ff, nt1, p.d_ff, p.rows,
-      static_cast<float*>(hidden), status);
-  note_launch();
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_kernel(expert_gemm_simt_kernel<true>, dim3(g1), dim3(256), 0, s, 1, pdl,
+                                static_cast<const float*>(x_packed), static_cast<const float*>(w_gate),
+                                static_cast<const float*>(w_up), offsets, p.E, p.hu, p.d_ff, nt1, p.d_ff, p.rows,
+                                static_cast<float*>(hidden), status);
   if (e != cudaSuccess) return e;
-  expert_gemm_simt_kernel<false><<<g2, 256, 0, s>>>(
-      static_cast<const float*>(hidden), static_cast<const float*>(w_down), nullptr, offsets, p.E,
-      p.d_ff, p.hu, nt2, p.hu, p.rows, static_cast<float*>(y_packed), status);
-  note_launch();
-  return cudaGetLastError();
+  return launch_kernel(expert_gemm_simt_kernel<false>, dim3(g2), dim3(256), 0, s, 1, true,
+                       static_cast<const float*>(hidden), static_cast<const float*>(w_down),
+                       static_cast<const float*>(nullptr), offsets, p.E, p.d_ff, p.hu, nt2, p.hu, p.rows,
+                       static_cast<float*>(y_packed), status);
 }
 
 }  // namespace moe

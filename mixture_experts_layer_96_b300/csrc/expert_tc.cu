@@ -78,11 +78,8 @@ expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
   const uint32_t done_bar = bar0 + 8u * (2 * kStages + 4);
 
   if (warp == 0) {
-    const bool ok = warp_tile_prefix(p.offsets, p.E, kBM, p.rows_cap, s_off, s_pre);
     if (lane == 0) {
-      s_ok = ok ? 1 : 0;
       s_abort = 0;
-      if (!ok && blockIdx.x == 0) set_status(p.status, kDevErrBadOffsets);
       for (int s = 0; s < kStages; ++s) {
         mbar_init(full_bar(s), 1);
         mbar_init(empty_bar(s), 1);
@@ -98,6 +95,13 @@ expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       if (EPI == kEpiSwiGLU) tma_prefetch_desc(&tmB1);
     }
     __syncwarp();
+    griddep_wait();  // the offsets and packed rows come from the previous kernel of the stream
+    const bool ok = warp_tile_prefix(p.offsets, p.E, kBM, p.rows_cap, s_off, s_pre);
+    if (lane == 0) {
+      s_ok = ok ? 1 : 0;
+      if (!ok && blockIdx.x == 0) set_status(p.status, kDevErrBadOffsets);
+    }
+    __syncwarp();
   } else if (warp == 1) {
     tmem_alloc(smem_addr(&s_tmem), kTmemCols);
     tmem_relinquish();
@@ -105,6 +109,8 @@ expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
   }
   __syncthreads();
   tc_fence_after();
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tmem_base = s_tmem;
   const bool valid = s_ok != 0;
   const int total = valid ? s_pre[p.E] * p.n_tiles : 0;
@@ -331,11 +337,8 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
   auto xch_bar = [&](int pair, int buf) { return bar0 + 8u * (2 * kPairStages + 5 + 2 * pair + buf); };
 
   if (warp == 0) {
-    const bool ok = warp_tile_prefix(p.offsets, p.E, kPairBM, p.rows_cap, s_off, s_pre);
     if (lane == 0) {
-      s_ok = ok ? 1 : 0;
       s_abort = 0;
-      if (!ok && blockIdx.x == 0) set_status(p.status, kDevErrBadOffsets);
       for (int s = 0; s < kPairStages; ++s) {
         mbar_init(full_bar(s), 1);
         mbar_init(empty_bar(s), 1);
@@ -356,6 +359,13 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
       }
     }
     __syncwarp();
+    griddep_wait();  // the offsets and packed rows come from the previous kernel of the stream
+    const bool ok = warp_tile_prefix(p.offsets, p.E, kPairBM, p.rows_cap, s_off, s_pre);
+    if (lane == 0) {
+      s_ok = ok ? 1 : 0;
+      if (!ok && blockIdx.x == 0) set_status(p.status, kDevErrBadOffsets);
+    }
+    __syncwarp();
   } else if (warp == 1) {
     tmem_alloc_pair(smem_addr(&s_tmem), kTmemCols);
     tmem_relinquish_pair();
@@ -364,6 +374,8 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
   __syncthreads();
   cluster_sync_all();  // the peer's barriers are initialised before any remote arrive or TMA
   tc_fence_after();
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tmem_base = s_tmem;
   const int total = s_ok ? s_pre[p.E] * p.n_tiles : 0;
   const int nkb = (p.K + kBK - 1) / kBK;
@@ -668,7 +680,7 @@ static int resident_cluster_grid(Kern kern, int cluster, size_t smem, int want) 
 template <int EPI>
 static cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                                   const CUtensorMap& s0, const CUtensorMap& s1, const TcParams& p,
-                                  int grid, cudaStream_t s) {
+                                  int grid, cudaStream_t s, bool pdl) {
   static bool attr_done[64] = {false};
   static int grid_cap[64] = {0};
   int dev = 0;
@@ -681,9 +693,9 @@ static cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b0, c
     attr_done[dev] = true;
   }
   if (dev < 64 && grid_cap[dev] > 0 && grid > grid_cap[dev]) grid = grid_cap[dev];
-  expert_gemm_tc_pair_kernel<EPI><<<grid, kTcThreads, kPairSmem, s>>>(a, b0, b1, s0, s1, p);
-  note_launch();
-  return cudaGetLastError();
+  // the 2-CTA cluster shape is compiled into the kernel
+  return launch_kernel(expert_gemm_tc_pair_kernel<EPI>, dim3(grid), dim3(kTcThreads), kPairSmem, s, 1, pdl, a, b0, b1,
+                       s0, s1, p);
 }
 
 // Pair tiles (256 rows) pay off when experts hold many rows; with few rows per expert (fine-grained
@@ -704,7 +716,7 @@ static int swap_max_rows(int K) {
 
 template <int EPI>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                             const TcParams& p, int grid, cudaStream_t s) {
+                             const TcParams& p, int grid, cudaStream_t s, bool pdl) {
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -714,21 +726,19 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const 
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  expert_gemm_tc_kernel<EPI><<<grid, kTcThreads, kTcSmem, s>>>(a, b0, b1, p);
-  note_launch();
-  return cudaGetLastError();
+  return launch_kernel(expert_gemm_tc_kernel<EPI>, dim3(grid), dim3(kTcThreads), kTcSmem, s, 1, pdl, a, b0, b1, p);
 }
 
 cudaError_t launch_expert_ffn_simt(const Problem& p, const void* x_packed, const int32_t* offsets,
                                    const void* w_gate, const void* w_up, const void* w_down,
-                                   void* hidden, void* y_packed, uint32_t* status, cudaStream_t s);
+                                   void* hidden, void* y_packed, uint32_t* status, cudaStream_t s, bool pdl);
 
 cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int32_t* offsets,
                               const void* w_gate, const void* w_up, const void* w_down,
                               void* hidden, void* y_packed, uint32_t* status, cudaStream_t s,
-                              void* save_gu) {
+                              void* save_gu, bool pdl) {
   if (!p.bf16)
-    return launch_expert_ffn_simt(p, x_packed, offsets, w_gate, w_up, w_down, hidden, y_packed, status, s);
+    return launch_expert_ffn_simt(p, x_packed, offsets, w_gate, w_up, w_down, hidden, y_packed, status, s, pdl);
   if (p.rows == 0) return cudaSuccess;
   CUtensorMap mA, mW1, mW3, mH, mW2;
   const uint64_t rows = (uint64_t)p.rows;
@@ -759,8 +769,8 @@ cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int3
   g.out = static_cast<__nv_bfloat16*>(hidden);
   g.swap_max = swap_max_rows(g.K);
   g.save_gu = static_cast<__nv_bfloat16*>(save_gu);
-  cudaError_t e = pair ? launch_tc_pair<kEpiSwiGLU>(mA, mW1, mW3, mW1s, mW3s, g, grid, s)
-                       : launch_tc<kEpiSwiGLU>(mA, mW1, mW3, g, grid, s);
+  cudaError_t e = pair ? launch_tc_pair<kEpiSwiGLU>(mA, mW1, mW3, mW1s, mW3s, g, grid, s, pdl)
+                       : launch_tc<kEpiSwiGLU>(mA, mW1, mW3, g, grid, s, pdl);
   if (e != cudaSuccess) return e;
   // down → y_packed
   g.K = p.d_ff;
@@ -770,8 +780,8 @@ cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int3
   g.out = static_cast<__nv_bfloat16*>(y_packed);
   g.swap_max = swap_max_rows(g.K);
   g.save_gu = nullptr;
-  return pair ? launch_tc_pair<kEpiPlain>(mH, mW2p, mW2p, mW2p, mW2p, g, grid, s)
-              : launch_tc<kEpiPlain>(mH, mW2, mW2, g, grid, s);
+  return pair ? launch_tc_pair<kEpiPlain>(mH, mW2p, mW2p, mW2p, mW2p, g, grid, s, true)
+              : launch_tc<kEpiPlain>(mH, mW2, mW2, g, grid, s, true);
 }
 
 }  // namespace moe

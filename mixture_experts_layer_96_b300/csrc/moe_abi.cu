@@ -11,8 +11,6 @@
 
 namespace moe {
 
-int route_block_units(int E);  // route.cu
-
 static std::atomic<uint64_t> g_launches{0};
 void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
@@ -116,9 +114,8 @@ moe_status_t make_problem(const moe_config_t* c, Problem* p) {
   if (!(cf > 0.0) || isinf(cf)) p->C = INT64_MAX;
   else p->C = (int64_t)ceil(cf * (double)c->K * (double)Tu / (double)c->E);
   p->rows = Tu * c->K;
+  p->ntiles = (Tu + kTileUnits - 1) / kTileUnits;
   p->nchunks = (Tu + kChunk - 1) / kChunk;
-  p->route_bt = route_block_units(c->E);
-  p->route_blocks = (Tu + p->route_bt - 1) / p->route_bt;
   p->elt = bf16 ? 2 : 4;
   return MOE_OK;
 }
@@ -135,19 +132,13 @@ WsLayout ws_layout(const Problem& p) {
   L.status = take(kWsAlign);
   L.counts = take(E * 4);
   L.offsets = take((E + 1) * 4);
-  L.chunk_hist = take((size_t)p.nchunks * E * 4);
-  L.chunk_base = take((size_t)p.nchunks * E * 4);
-  L.psum_part = take((size_t)p.route_blocks * E * 4);
-  L.cnt_part = take((size_t)p.route_blocks * E * 4);
+  L.chunk_hist = take((size_t)p.ntiles * E * 4);
+  L.chunk_base = take((size_t)p.ntiles * E * 4);
+  L.psum = take((size_t)p.ntiles * E * 4);
   L.aux_terms = take(E * 8);
-  if (p.bf16) {
-    const RouterPlan r = router_plan(p);
-    L.router_wt = take((size_t)r.N * p.hu * 2);
-    L.router_part = take((size_t)r.splits * (size_t)p.Tu * E * 4);
-  } else {
-    L.router_wt = off;
-    L.router_part = take((size_t)p.Tu * E * 4);
-  }
+  L.w_pad = take(p.bf16 ? (size_t)p.hu * ((E + 7) / 8 * 8) * 2 : 0);
+  L.logits = take(p.bf16 ? 0 : (size_t)p.Tu * E * 4);
+  L.rank = take(TK * 4);
   L.idx = take(TK * 4);
   L.gate = take(TK * 4);
   L.slot_of = take(TK * 4);
@@ -169,6 +160,7 @@ struct BwdLayout {
   size_t wg_part;    // fp32 [chunks][h'][E]
   size_t dy_t;       // bf16 [h'][padded cols]  dY_packed transposed, experts padded to 64 rows
   size_t x_t;        // bf16 [h'][padded cols]  X_packed transposed, likewise
+  size_t wgt;        // bf16 [E][h']            W_g transposed (for dx += dl·W_gᵀ)
   size_t total;
 };
 
@@ -189,6 +181,7 @@ static BwdLayout bwd_layout(const Problem& p) {
   L.wg_part = take((size_t)backward_wg_chunks(p) * p.hu * p.E * 4);
   L.dy_t = take((size_t)p.hu * (size_t)backward_padded_cols(p) * 2);
   L.x_t = take((size_t)p.hu * (size_t)backward_padded_cols(p) * 2);
+  L.wgt = take((size_t)p.E * p.hu * 2);
   L.total = off;
   return L;
 }
@@ -242,6 +235,53 @@ moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, moe_stream_t 
   return cuda_status(cudaMemsetAsync(ws, 0, kWsAlign, (cudaStream_t)stream));
 }
 
+}  // extern "C"
+
+namespace moe {
+
+// The routing kernel(s) of a call: bf16 → the fused tensor-core kernel; fp32 → the CUDA-core
+// router into the workspace, then routing from those logits; given logits → routing from them.
+// Leaves each tile's counts and Σp in the workspace and each pick's place in its tile in rank_out.
+static cudaError_t route_stage(const Problem& p, const void* x, const void* w_router, const float* logits_in,
+                               const float* logit_bias, const float* select_bias, int32_t* idx, float* gate,
+                               float* logits_out, int32_t* rank_out, void* ws, cudaStream_t s) {
+  if (p.Tu == 0) return cudaSuccess;
+  const WsLayout L = ws_layout(p);
+  SelectCtx sel;
+  sel.select_bias = p.sigmoid ? select_bias : nullptr;
+  sel.idx = idx;
+  sel.gate = gate;
+  sel.E = p.E;
+  sel.K = p.K;
+  sel.n_groups = p.n_groups;
+  sel.topk_groups = p.topk_groups;
+  int32_t* hist = ws_ptr<int32_t>(ws, L.chunk_hist);
+  float* psum = ws_ptr<float>(ws, L.psum);
+  if (logits_in)
+    return launch_select_logits(p, logits_in, logit_bias, sel, nullptr, rank_out, hist, psum, s, false);
+  if (p.bf16)
+    return launch_route_tc(p, x, w_router, logit_bias, sel, logits_out, rank_out, hist, psum,
+                           ws_ptr<void>(ws, L.w_pad), ws_ptr<uint32_t>(ws, L.status), s);
+  float* lg = ws_ptr<float>(ws, L.logits);
+  cudaError_t e = launch_router_simt_logits(p, x, w_router, lg, s);
+  if (e != cudaSuccess) return e;
+  return launch_select_logits(p, lg, logit_bias, sel, logits_out, rank_out, hist, psum, s, true);
+}
+
+// The per-expert scan over the routing tiles (counts, offsets, tile bases) and the aux loss.
+static cudaError_t scan_stage(const Problem& p, void* ws, int32_t* counts_out, int32_t* offsets_out, float* aux_out,
+                              cudaStream_t s) {
+  const WsLayout L = ws_layout(p);
+  return launch_scan(p, p.ntiles, ws_ptr<int32_t>(ws, L.chunk_hist), aux_out ? ws_ptr<float>(ws, L.psum) : nullptr,
+                     ws_ptr<int32_t>(ws, L.chunk_base), ws_ptr<int32_t>(ws, L.counts), ws_ptr<int32_t>(ws, L.offsets),
+                     counts_out, offsets_out, ws_ptr<double>(ws, L.aux_terms),
+                     ws_ptr<unsigned int>(ws, L.status + 8), aux_out, s, true);
+}
+
+}  // namespace moe
+
+extern "C" {
+
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_router,
                        const float* logit_bias, const float* select_bias, int32_t* topk_idx,
                        float* topk_gate, float* logits_out, float* aux_out, void* ws,
@@ -251,8 +291,13 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_rou
   if (st != MOE_OK) return st;
   if (!ws_ok(ws)) return MOE_ERR_WORKSPACE;
   if (p.Tu > 0 && (!x || !w_router || !topk_idx || !topk_gate)) return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_route(p, x, w_router, nullptr, logit_bias, select_bias, topk_idx,
-                                  topk_gate, logits_out, aux_out, ws, (cudaStream_t)stream));
+  if (p.Tu > 0 && p.bf16 && !aligned16(x)) return MOE_ERR_INVALID_ARG;
+  const cudaStream_t s = (cudaStream_t)stream;
+  const WsLayout L = ws_layout(p);
+  cudaError_t e = route_stage(p, x, w_router, nullptr, logit_bias, select_bias, topk_idx, topk_gate, logits_out,
+                              ws_ptr<int32_t>(ws, L.rank), ws, s);
+  if (e != cudaSuccess || !aux_out) return cuda_status(e);
+  return cuda_status(scan_stage(p, ws, nullptr, nullptr, aux_out, s));
 }
 
 moe_status_t moe_route_logits(const moe_config_t* cfg, const float* logits, const float* logit_bias,
@@ -263,8 +308,12 @@ moe_status_t moe_route_logits(const moe_config_t* cfg, const float* logits, cons
   if (st != MOE_OK) return st;
   if (!ws_ok(ws)) return MOE_ERR_WORKSPACE;
   if (p.Tu > 0 && (!logits || !topk_idx || !topk_gate)) return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_route(p, nullptr, nullptr, logits, logit_bias, select_bias, topk_idx,
-                                  topk_gate, nullptr, aux_out, ws, (cudaStream_t)stream));
+  const cudaStream_t s = (cudaStream_t)stream;
+  const WsLayout L = ws_layout(p);
+  cudaError_t e = route_stage(p, nullptr, nullptr, logits, logit_bias, select_bias, topk_idx, topk_gate, nullptr,
+                              ws_ptr<int32_t>(ws, L.rank), ws, s);
+  if (e != cudaSuccess || !aux_out) return cuda_status(e);
+  return cuda_status(scan_stage(p, ws, nullptr, nullptr, aux_out, s));
 }
 
 moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
@@ -276,8 +325,16 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   if (!ws_ok(ws)) return MOE_ERR_WORKSPACE;
   if (!offsets) return MOE_ERR_INVALID_ARG;
   if (p.Tu > 0 && (!x || !topk_idx || !slot_of || !row_token || !x_packed)) return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_dispatch(p, x, topk_idx, counts, offsets, slot_of, row_token, x_packed,
-                                     ws, (cudaStream_t)stream));
+  const WsLayout L = ws_layout(p);
+  DispatchScratch sc;
+  sc.chunk_hist = ws_ptr<int32_t>(ws, L.chunk_hist);
+  sc.chunk_base = ws_ptr<int32_t>(ws, L.chunk_base);
+  sc.counts = ws_ptr<int32_t>(ws, L.counts);
+  sc.offsets = ws_ptr<int32_t>(ws, L.offsets);
+  sc.ticket = ws_ptr<unsigned int>(ws, L.status + 8);
+  sc.status = ws_ptr<uint32_t>(ws, L.status);
+  return cuda_status(launch_dispatch_from_idx(p, x, topk_idx, counts, offsets, slot_of, row_token, x_packed, sc,
+                                              (cudaStream_t)stream));
 }
 
 moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_packed, const int32_t* offsets,
@@ -320,6 +377,7 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const void* x, const m
   if (p.Tu > 0 && (!x || !y)) return MOE_ERR_INVALID_ARG;
   if (p.bf16 && !(aligned16(w->w_gate) && aligned16(w->w_up) && aligned16(w->w_down)))
     return MOE_ERR_INVALID_ARG;
+  if (p.Tu > 0 && p.bf16 && !aligned16(x)) return MOE_ERR_INVALID_ARG;
   moe_outputs_t none;
   memset(&none, 0, sizeof(none));
   const moe_outputs_t& o = out ? *out : none;
@@ -335,17 +393,22 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const void* x, const m
   void* y_packed = ws_ptr<void>(ws, L.y_packed);
   uint32_t* status = ws_ptr<uint32_t>(ws, L.status);
 
-  cudaError_t e = launch_route(p, x, w->w_router, nullptr, w->logit_bias, w->select_bias, idx, gate,
-                               o.logits, o.aux, ws, s);
+  // routing (each pick's place within its tile goes into slot_of, which the pack turns into slots)
+  cudaError_t e = route_stage(p, x, w->w_router, nullptr, w->logit_bias, w->select_bias, idx, gate, o.logits, slot_of,
+                              ws, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  // the scan writes the offsets into the workspace; the caller's copy is optional
-  e = launch_dispatch(p, x, idx, o.counts, o.offsets ? o.offsets : offsets_ws, slot_of, row_token,
-                      x_packed, ws, s);
+  // counts, offsets (into the workspace; the caller's copies are optional) and the aux loss
+  e = scan_stage(p, ws, o.counts, o.offsets, o.aux, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (p.rows > 0) {
+    e = launch_pack(p, x, idx, kTileShift, ws_ptr<int32_t>(ws, L.chunk_base), offsets_ws, slot_of, row_token, x_packed,
+                    s, true);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
   e = launch_expert_ffn(p, x_packed, offsets_ws, w->w_gate, w->w_up, w->w_down, hidden, y_packed,
-                        status, s, gu);
+                        status, s, gu, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = launch_combine(p, y_packed, slot_of, gate, y, status, s);
+  e = launch_combine(p, y_packed, slot_of, gate, y, status, s, true);
   return cuda_status(e);
 }
 
@@ -423,7 +486,9 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_backward_router(p, x, dl, backward_wg_chunks(p), ws_ptr<float>(bws, B.wg_part), grads->dw_router, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = launch_backward_dx(p, dx_packed, out->slot_of, dl, ws_ptr<void>(ws, L.router_wt), grads->dx, s);
+  e = launch_router_transpose(p, w->w_router, ws_ptr<void>(bws, B.wgt), s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_backward_dx(p, dx_packed, out->slot_of, dl, ws_ptr<void>(bws, B.wgt), grads->dx, s);
   return cuda_status(e);
 }
 

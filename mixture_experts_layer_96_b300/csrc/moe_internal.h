@@ -14,9 +14,11 @@ namespace moe {
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
 constexpr int kMaxGroups = 32;
-constexpr int kChunk = 256;          // units per dispatch chunk (one block, one thread per unit)
+constexpr int kTileUnits = 128;      // units per routing tile (one router M tile); a dispatch chunk
+constexpr int kTileShift = 7;
+constexpr int kChunk = 256;          // units per chunk when the dispatch ranks given picks
+constexpr int kChunkShift = 8;
 constexpr size_t kWsAlign = 1024;
-constexpr int kRouterSplitTarget = 160;  // aim for about this many router CTAs (>= SMs of a B300)
 
 // A validated configuration with the derived sizes every launcher needs.
 struct Problem {
@@ -29,30 +31,38 @@ struct Problem {
   bool sigmoid;
   int64_t C;         // capacity, or INT64_MAX for no drop
   int64_t rows;      // packed-row capacity T'·K
-  int64_t nchunks;   // ceil(T'/kChunk)
-  int route_bt;      // units per router block
-  int64_t route_blocks;
+  int64_t ntiles;    // ceil(T'/kTileUnits): routing tiles
+  int64_t nchunks;   // ceil(T'/kChunk): chunks of the dispatch from given picks
   size_t elt;        // bytes per activation/weight element (2 or 4)
 };
 
-// Tensor-core router GEMM plan: N = E rounded up to 16, K split into `splits` slices.
-struct RouterPlan {
-  int N, m_tiles, nkb, kb_per_split, splits;
+// Routing of one tile of units (select_tile.cuh): where the picks and gates go.
+struct SelectCtx {
+  const float* select_bias;  // [E] or null (sigmoid only)
+  int32_t* idx;              // [T'][K]
+  float* gate;               // [T'][K]
+  int E, K, n_groups, topk_groups;
 };
-RouterPlan router_plan(const Problem& p);
+
+// Tensor-core router plan (route_tc.cu): MMA N = 64·nblk; a cluster of S CTAs per 128-unit tile,
+// each over kbs of the nkb 64-wide k-blocks.
+struct RouterPlan {
+  int nblk, Np, m_tiles, nkb, S, kbs;
+};
+RouterPlan router_plan(const Problem& p, int sms);
 
 // Offsets (bytes) of the workspace regions; every region starts 1024-byte aligned.
 struct WsLayout {
-  size_t status;       // uint32 status word at +0, uint32 aux finalize ticket at +4
+  size_t status;       // uint32 status word at +0, uint32 scan ticket at +8
   size_t counts;       // int32 [E]
   size_t offsets;      // int32 [E+1]
-  size_t chunk_hist;   // int32 [nchunks][E]
-  size_t chunk_base;   // int32 [nchunks][E]
-  size_t psum_part;    // float [route_blocks][E]
-  size_t cnt_part;     // int32 [route_blocks][E]
+  size_t chunk_hist;   // int32 [ntiles][E] picks per expert of each tile / chunk
+  size_t chunk_base;   // int32 [ntiles][E] each tile's / chunk's base in the expert queues
+  size_t psum;         // float [ntiles][E] Σ over the tile's units of p_{t,e}
   size_t aux_terms;    // double [E] per-expert aux terms
-  size_t router_wt;    // bf16 [N][h'] transposed router weight (bf16 layers)
-  size_t router_part;  // float [splits][T'][E] partial logits (bf16 layers)
+  size_t w_pad;        // bf16 [h'][E rounded up to 8] router weight copy (bf16 layers, when needed)
+  size_t logits;       // float [T'][E] router logits (fp32 layers)
+  size_t rank;         // int32 [T'][K] pick places within their tile (routing calls alone)
   size_t idx;          // int32 [T'][K]
   size_t gate;         // float [T'][K]
   size_t slot_of;      // int32 [T'][K]
@@ -61,6 +71,17 @@ struct WsLayout {
   size_t hidden;       // elt [T'K][d_ff]
   size_t y_packed;     // elt [T'K][h']
   size_t total;
+};
+
+// Scratch of the dispatch from given picks (workspace regions, or the fixed array of the
+// allocation-free call).
+struct DispatchScratch {
+  int32_t* chunk_hist;   // [nchunks][E]
+  int32_t* chunk_base;   // [nchunks][E]
+  int32_t* counts;       // [E]
+  int32_t* offsets;      // [E+1]
+  unsigned int* ticket;  // zero between calls
+  uint32_t* status;      // or null
 };
 
 moe_status_t make_problem(const moe_config_t* cfg, Problem* p);
@@ -76,6 +97,38 @@ int device_sm_count();
 
 // Counts every kernel this library enqueues.
 void note_launch(int n = 1);
+
+// Launch `kern` on `s` and return that launch's own error (no earlier error is picked up).
+// cluster > 1: thread-block clusters of that many CTAs along x. pdl: programmatic dependent launch
+// (the kernel may start before the previous kernel of the stream ends; it must call griddep_wait
+// before reading anything that kernel writes, or writing anything it reads).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          unsigned cluster, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  unsigned n = 0;
+  if (cluster > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = cluster;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  note_launch();
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
 
 // Tensor-map encoding through the driver entry point (no link-time libcuda dependency).
 bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
@@ -93,23 +146,39 @@ bool encode_tmap_3d_f32_sw128(CUtensorMap* map, const void* base, uint64_t d0, u
                               uint32_t box0, uint32_t box1);
 
 // ---- launchers (return cudaSuccess or the launch error) --------------------------------------
-cudaError_t launch_route(const Problem& p, const void* x, const void* w_router,
-                         const float* logits_in, const float* logit_bias, const float* select_bias,
-                         int32_t* idx, float* gate, float* logits_out, float* aux_out, void* ws,
-                         cudaStream_t s);
+// pdl: the launch may overlap the previous kernel of the stream (see launch_kernel).
 
-cudaError_t launch_router_tc(const Problem& p, const void* x, const void* w_router, void* wt, float* part,
-                             uint32_t* status, cudaStream_t s);
-
-cudaError_t launch_dispatch(const Problem& p, const void* x, const int32_t* idx, int32_t* counts,
-                            int32_t* offsets, int32_t* slot_of, int32_t* row_token, void* x_packed,
-                            void* ws, cudaStream_t s);
+// bf16 layers: router GEMM + routing of each 128-unit tile in one kernel (plus a padded copy of W_g
+// into w_pad first when E % 8 != 0 or W_g is not 16-byte aligned).
+cudaError_t launch_route_tc(const Problem& p, const void* x, const void* w_router, const float* logit_bias,
+                            const SelectCtx& sel, float* logits_out, int32_t* rank_out, int32_t* tile_hist,
+                            float* tile_psum, void* w_pad, uint32_t* status, cudaStream_t s);
+// fp32 layers: router logits [T'][E] on the CUDA cores.
+cudaError_t launch_router_simt_logits(const Problem& p, const void* x, const void* w, float* logits, cudaStream_t s);
+// Routing of each 128-unit tile from given fp32 logits (the logit bias added in fp32).
+cudaError_t launch_select_logits(const Problem& p, const float* logits, const float* logit_bias, const SelectCtx& sel,
+                                 float* logits_out, int32_t* rank_out, int32_t* tile_hist, float* tile_psum,
+                                 cudaStream_t s, bool pdl);
+// Per expert: chunk bases, pre-drop counts, offsets; the aux loss when psum and aux_out are given.
+cudaError_t launch_scan(const Problem& p, int64_t nchunks, const int32_t* hist, const float* psum,
+                        int32_t* chunk_base, int32_t* counts_ws, int32_t* offsets_ws, int32_t* counts_out,
+                        int32_t* offsets_out, double* terms, unsigned int* ticket, float* aux_out, cudaStream_t s,
+                        bool pdl);
+// Slots of the picks (slot_of holds the places within chunks of 2^chunk_shift units on entry) and
+// the packed rows.
+cudaError_t launch_pack(const Problem& p, const void* x, const int32_t* idx, int chunk_shift, const int32_t* chunk_base,
+                        const int32_t* offsets, int32_t* slot_of, int32_t* row_token, void* x_packed, cudaStream_t s,
+                        bool pdl);
+// The whole dispatch from given picks: chunk ranks, scan, pack.
+cudaError_t launch_dispatch_from_idx(const Problem& p, const void* x, const int32_t* idx, int32_t* counts_out,
+                                     int32_t* offsets_out, int32_t* slot_of, int32_t* row_token, void* x_packed,
+                                     const DispatchScratch& sc, cudaStream_t s);
 
 // save_gu (bf16 layers): also write the SwiGLU inputs G | U as bf16 [rows][2·d_ff] for the backward.
 cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int32_t* offsets,
                               const void* w_gate, const void* w_up, const void* w_down,
                               void* hidden, void* y_packed, uint32_t* status, cudaStream_t s,
-                              void* save_gu = nullptr);
+                              void* save_gu = nullptr, bool pdl = false);
 
 // ---- backward (bf16 layers, h' and d_ff multiples of 64) ---------------------------------------
 cudaError_t launch_expert_ffn_backward(const Problem& p, const int32_t* offsets, const void* x_packed,
@@ -127,10 +196,12 @@ cudaError_t launch_backward_logits(const Problem& p, const float* logits, const 
 int backward_wg_chunks(const Problem& p);
 cudaError_t launch_backward_router(const Problem& p, const void* x, const float* dl, int nchunks, float* part,
                                    float* dw_router, cudaStream_t s);
+// W_gᵀ [E][h'] (bf16) for dx += dl·W_gᵀ.
+cudaError_t launch_router_transpose(const Problem& p, const void* w_router, void* wt, cudaStream_t s);
 cudaError_t launch_backward_dx(const Problem& p, const void* dx_packed, const int32_t* slot_of, const float* dl,
                                const void* w_router_t, void* dx, cudaStream_t s);
 
 cudaError_t launch_combine(const Problem& p, const void* y_packed, const int32_t* slot_of,
-                           const float* gate, void* y, uint32_t* status, cudaStream_t s);
+                           const float* gate, void* y, uint32_t* status, cudaStream_t s, bool pdl = false);
 
 }  // namespace moe

@@ -1,18 +1,25 @@
-// Router logits for fp32 layers on the CUDA cores: l = x·W_g, written as fp32 [T'][E] for the
-// selection kernel (route_select.cu); bf16 layers use the tensor-core GEMM (route_tc.cu). Also
-// the aux-loss reduction, and launch_route, which runs the router and the selection.
-//   [Lesson 10 "专家并行 EP", §1: affinity scores x·W_g; §4: L_aux = α·E·Σ f_i·P_i]
+// Routing of fp32 layers, and routing from given logits.
+//   [Lesson 10 "专家并行 EP", §1: affinity scores x·W_g, s(x) = Softmax(TopK(x·W_g, K)) or sigmoid;
+//    §4: L_aux = α·E·Σ f_i·P_i]
 //
-// Block = 256 threads, BT units; the [BT][EP] logit tile (EP = E rounded up to a power of two
-// >= 8) is accumulated with fp32 FMAs over 32-column steps of h' staged in shared memory; for
-// small E the block splits the reduction dimension over warp groups and adds the slices in a
-// fixed order.
+// fp32 layers: router_gemm_simt_kernel computes l = x·W_g on the CUDA cores into the workspace
+// (bf16 layers use the tensor-core kernel of route_tc.cu, which routes in its epilogue). Block =
+// 256 threads, BT units; the [BT][EP] logit tile (EP = E rounded up to a power of two >= 8) is
+// accumulated with fp32 FMAs over 32-column steps of h' staged in shared memory; for small E the
+// block splits the reduction dimension over warp groups and adds the slices in a fixed order.
+//
+// select_logits_kernel routes from fp32 logits [T'][E]: a block per 128 units stages the logits
+// plus the logit bias (added in fp32) in shared memory and runs the same tile routing as the fused
+// kernel (select_tile.cuh), so both leave the same per-tile counts, Σp and pick places for the
+// dispatch and the aux loss.
 #include <math.h>
 
 #include "moe_device.cuh"
 #include "moe_internal.h"
+#include "select_tile.cuh"
 
 namespace moe {
+
 
 constexpr int kRouteThreads = 256;
 constexpr int kRouteBK = 32;
@@ -170,51 +177,97 @@ router_gemm_simt_kernel(RouteArgs a) {
   }
 }
 
-// aux = α·E·Σ_i (count_i/(T'·K))·(ΣP_i/T')  [Lesson 10 §4]. One block per expert reduces that
-// expert's per-block partials (fixed strided order, then a fixed tree, in fp64); the last block
-// to finish (ticket counter) adds the E terms in expert order and resets the ticket.
-__global__ void __launch_bounds__(256)
-aux_finalize_kernel(const float* __restrict__ psum_part, const int32_t* __restrict__ cnt_part,
-                    int64_t blocks, int E, int64_t Tu, int K, float alpha, double* terms,
-                    unsigned int* ticket, float* aux_out) {
-  __shared__ double sP[256];
-  __shared__ long long sC[256];
-  __shared__ bool last;
-  const int tid = threadIdx.x, e = blockIdx.x;
-  double P = 0.0;
-  long long c = 0;
-  for (int64_t b = tid; b < blocks; b += 256) {
-    P += (double)psum_part[b * E + e];
-    c += cnt_part[b * E + e];
+namespace {
+
+constexpr int kSelThreads = 256;
+
+struct SelLogitsArgs {
+  const float* logits;      // [T'][E]
+  const float* logit_bias;  // [E] or null
+  float* logits_out;        // [T'][E] or null (logits with the bias)
+  SelectCtx sel;
+  int32_t* rank_out;        // [T'][K]
+  int32_t* tile_hist;       // [tiles][E]
+  float* tile_psum;         // [tiles][E]
+  int64_t Tu;
+};
+
+struct SelEpi {
+  int ldl;
+  size_t lg, picks, rank, lanes, wpre, gscr, psum, hist, scratch, total;
+};
+
+inline SelEpi sel_epi(int E, int epl) {
+  SelEpi L;
+  L.ldl = E + 1;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { const size_t at = off; off = (off + bytes + 15) / 16 * 16; return at; };
+  L.lg = take((size_t)kTileUnits * L.ldl * 4);
+  L.picks = take((size_t)kTileUnits * kPickStride * 4);
+  L.rank = take((size_t)kTileUnits * kPickStride * 4);
+  L.lanes = take((size_t)(kSelThreads / 32) * E * 4);
+  L.wpre = take((size_t)(kSelThreads / 32) * E * 4);
+  L.gscr = take(epl > 0 ? (size_t)(kSelThreads / 32) * 32 * epl * 8 : 0);
+  L.psum = take((size_t)E * 4);
+  L.hist = take((size_t)E * 4);
+  L.scratch = take((size_t)kSelThreads * 4);
+  L.total = off;
+  return L;
+}
+
+template <int EPL, int KMAX, bool SIGMOID>
+__global__ void __launch_bounds__(kSelThreads)
+select_logits_kernel(SelLogitsArgs a, SelEpi L) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  griddep_launch_dependents();
+  griddep_wait();
+  const int tid = threadIdx.x, E = a.sel.E, K = a.sel.K, ldl = L.ldl;
+  const int64_t u0 = (int64_t)blockIdx.x * kTileUnits;
+  const int R = (int)min((int64_t)kTileUnits, a.Tu - u0);
+  float* lg = reinterpret_cast<float*>(smem_raw + L.lg);
+  for (int i = tid; i < R * E; i += kSelThreads) {
+    const int r = i / E, e = i - r * E;
+    float v = a.logits[(u0 + r) * E + e];
+    if (a.logit_bias) v = v + a.logit_bias[e];
+    lg[r * ldl + e] = v;
+    if (a.logits_out) a.logits_out[(u0 + r) * E + e] = v;
   }
-  sP[tid] = P;
-  sC[tid] = c;
   __syncthreads();
-  for (int s = 128; s; s >>= 1) {
-    if (tid < s) {
-      sP[tid] += sP[tid + s];
-      sC[tid] += sC[tid + s];
-    }
-    __syncthreads();
-  }
-  if (tid == 0) {
-    terms[e] = Tu > 0 ? ((double)sC[0] / ((double)Tu * K)) * (sP[0] / (double)Tu) : 0.0;
-    __threadfence();
-    last = atomicAdd(ticket, 1u) == (unsigned)(E - 1);
-  }
+  int* picks = reinterpret_cast<int*>(smem_raw + L.picks);
+  int* rank = reinterpret_cast<int*>(smem_raw + L.rank);
+  float* psum_s = reinterpret_cast<float*>(smem_raw + L.psum);
+  int* hist_s = reinterpret_cast<int*>(smem_raw + L.hist);
+  if constexpr (EPL == 0)
+    select_rows_thread<KMAX, SIGMOID>(a.sel, lg, ldl, R, u0, picks);
+  else
+    select_rows_warp<EPL, SIGMOID>(a.sel, lg, ldl, R, u0, picks, smem_raw + L.gscr);
   __syncthreads();
-  if (last) {
-    __threadfence();
-    const volatile double* vt = terms;
-    for (int i = tid; i < E; i += 256) sP[i] = vt[i];  // all E terms, loaded in parallel
-    __syncthreads();
-    if (tid == 0) {
-      double acc = 0.0;
-      for (int i = 0; i < E; ++i) acc += sP[i];  // expert order
-      *aux_out = (float)((double)alpha * E * acc);
-      *ticket = 0u;
-    }
+  column_sums(lg, ldl, R, E, psum_s, reinterpret_cast<float*>(smem_raw + L.scratch));
+  rank_picks(picks, R, K, E, rank, hist_s, reinterpret_cast<uint32_t*>(smem_raw + L.lanes),
+             reinterpret_cast<int*>(smem_raw + L.wpre));
+  for (int e = tid; e < E; e += kSelThreads) {
+    a.tile_hist[(int64_t)blockIdx.x * E + e] = hist_s[e];
+    a.tile_psum[(int64_t)blockIdx.x * E + e] = psum_s[e];
   }
+  for (int i = tid; i < R * K; i += kSelThreads) {
+    const int t = i / K, k = i - t * K;
+    a.rank_out[(u0 + t) * K + k] = rank[t * kPickStride + k];
+  }
+}
+
+template <int EPL, int KMAX, bool SIGMOID>
+cudaError_t launch_sel(const SelLogitsArgs& a, const SelEpi& L, unsigned grid, cudaStream_t s, bool pdl) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(select_logits_kernel<EPL, KMAX, SIGMOID>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  return launch_kernel(select_logits_kernel<EPL, KMAX, SIGMOID>, dim3(grid), dim3(kSelThreads), L.total, s, 1, pdl,
+                       a, L);
 }
 
 template <int EP>
@@ -229,9 +282,8 @@ static cudaError_t launch_router_simt_t(const RouteArgs& a, int64_t blocks, cuda
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  router_gemm_simt_kernel<float, EP><<<(unsigned)blocks, kRouteThreads, Tl::SMEM, s>>>(a);
-  note_launch();
-  return cudaGetLastError();
+  return launch_kernel(router_gemm_simt_kernel<float, EP>, dim3((unsigned)blocks), dim3(kRouteThreads), Tl::SMEM, s,
+                       1, false, a);
 }
 
 static cudaError_t launch_router_simt(const Problem& p, const void* x, const void* w, float* logits,
@@ -256,49 +308,42 @@ static cudaError_t launch_router_simt(const Problem& p, const void* x, const voi
   }
 }
 
-int select_block_units(int E);  // route_select.cu
-int route_block_units(int E) { return select_block_units(E); }
+}  // namespace
 
-cudaError_t launch_select(const Problem& p, const float* logits, int nparts, int64_t part_stride,
-                          const float* logit_bias, const float* select_bias, int32_t* idx, float* gate,
-                          float* logits_out, float* psum_part, int32_t* cnt_part, cudaStream_t s);
+cudaError_t launch_select_logits(const Problem& p, const float* logits, const float* logit_bias, const SelectCtx& sel,
+                                 float* logits_out, int32_t* rank_out, int32_t* tile_hist, float* tile_psum,
+                                 cudaStream_t s, bool pdl) {
+  if (p.Tu == 0) return cudaSuccess;
+  SelLogitsArgs a;
+  a.logits = logits;
+  a.logit_bias = logit_bias;
+  a.logits_out = logits_out;
+  a.sel = sel;
+  a.rank_out = rank_out;
+  a.tile_hist = tile_hist;
+  a.tile_psum = tile_psum;
+  a.Tu = p.Tu;
+  const bool warp_sel = p.E > 64;
+  const int epl = !warp_sel ? 0 : (p.E <= 128 ? 4 : 8);
+  const SelEpi L = sel_epi(p.E, epl);
+  const unsigned grid = (unsigned)p.ntiles;
+  const int kb = p.K <= 2 ? 2 : (p.K <= 4 ? 4 : 8);
+  if (warp_sel) {
+    if (epl == 4) return p.sigmoid ? launch_sel<4, 8, true>(a, L, grid, s, pdl) : launch_sel<4, 8, false>(a, L, grid, s, pdl);
+    return p.sigmoid ? launch_sel<8, 8, true>(a, L, grid, s, pdl) : launch_sel<8, 8, false>(a, L, grid, s, pdl);
+  }
+  if (p.sigmoid) {
+    if (kb == 2) return launch_sel<0, 2, true>(a, L, grid, s, pdl);
+    if (kb == 4) return launch_sel<0, 4, true>(a, L, grid, s, pdl);
+    return launch_sel<0, 8, true>(a, L, grid, s, pdl);
+  }
+  if (kb == 2) return launch_sel<0, 2, false>(a, L, grid, s, pdl);
+  if (kb == 4) return launch_sel<0, 4, false>(a, L, grid, s, pdl);
+  return launch_sel<0, 8, false>(a, L, grid, s, pdl);
+}
 
-cudaError_t launch_route(const Problem& p, const void* x, const void* w_router,
-                         const float* logits_in, const float* logit_bias, const float* select_bias,
-                         int32_t* idx, float* gate, float* logits_out, float* aux_out, void* ws,
-                         cudaStream_t s) {
-  const WsLayout L = ws_layout(p);
-  float* psum_part = ws_ptr<float>(ws, L.psum_part);
-  int32_t* cnt_part = ws_ptr<int32_t>(ws, L.cnt_part);
-  cudaError_t e = cudaSuccess;
-  if (p.Tu > 0) {
-    const float* logits = logits_in;
-    int nparts = 1;
-    if (!logits_in) {
-      float* part = ws_ptr<float>(ws, L.router_part);
-      if (p.bf16) {
-        // x·W_g on the tensor cores, as K-slice partial sums
-        e = launch_router_tc(p, x, w_router, ws_ptr<void>(ws, L.router_wt), part,
-                             ws_ptr<uint32_t>(ws, L.status), s);
-        nparts = router_plan(p).splits;
-      } else {
-        e = launch_router_simt(p, x, w_router, part, s);
-      }
-      if (e != cudaSuccess) return e;
-      logits = part;
-    }
-    e = launch_select(p, logits, nparts, p.Tu * p.E, logit_bias, select_bias, idx, gate, logits_out,
-                      psum_part, cnt_part, s);
-    if (e != cudaSuccess) return e;
-  }
-  if (aux_out) {
-    aux_finalize_kernel<<<p.E, 256, 0, s>>>(psum_part, cnt_part, p.route_blocks, p.E, p.Tu, p.K,
-                                            p.cfg.aux_alpha, ws_ptr<double>(ws, L.aux_terms),
-                                            ws_ptr<unsigned int>(ws, L.status + 4), aux_out);
-    note_launch();
-    e = cudaGetLastError();
-  }
-  return e;
+cudaError_t launch_router_simt_logits(const Problem& p, const void* x, const void* w, float* logits, cudaStream_t s) {
+  return launch_router_simt(p, x, w, logits, s);
 }
 
 }  // namespace moe

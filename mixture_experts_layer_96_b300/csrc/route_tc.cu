@@ -1,62 +1,111 @@
-// Router logits on the tensor cores (bf16 layers): l = x·W_g as a dense GEMM
-// [T'][h'] x [h'][E] → fp32, written as partial sums of K slices; the selection kernel
-// (route.cu, logits path) adds the slices in a fixed order, adds the logit bias and routes.
-//   [Lesson 10 "专家并行 EP", §1: affinity scores x·W_g]
+// Routing of bf16 layers in one kernel: router logits on the tensor cores, then scores, group limit,
+// Top-K, gates, the aux-loss statistics and the dispatch's per-tile counts in the epilogue.
+//   [Lesson 10 "专家并行 EP", §1: affinity scores x·W_g, s(x) = Softmax(TopK(x·W_g, K)) or sigmoid;
+//    §4: L_aux = α·E·Σ f_i·P_i; §5: node-limited (group-limited) routing]
 //
-// W_g is kept in the pages' [h'][E] orientation by the caller; a small kernel writes its
-// transpose W_gᵀ [N][h'] (N = E rounded up to a multiple of 16, zero rows past E) into the
-// workspace, the K-major B operand the MMA wants.
+// A cluster of S CTAs (S = 1, 2, 4 or 8) owns one tile of 128 units. CTA r of the cluster computes
+// the partial logits of the tile over its slice of the reduction dimension h' with tcgen05.mma
+// (M = 128 units, N = E rounded up to 64, K = 16): x comes K-major through TMA (128 x 64 boxes,
+// 128-byte swizzle); W_g is read in the pages' own [h'][E] orientation, which is the MN-major
+// layout of the B operand, through TMA boxes of 64 experts x 64 rows (experts past E read as
+// zeros), so no transposed copy of W_g is made. Then, in column passes of 64 experts:
+//   - every CTA copies its TMEM partial to shared memory;
+//   - CTA r adds the S partials of its own 128/S units in cluster-rank order (reading the peers'
+//     shared memory through the cluster window), adds the logit bias, and writes the logits;
+// so the sum is deterministic and no partial logits go through HBM. Each CTA then routes its units
+// (select_tile.cuh) and counts its picks per expert; the cluster adds the counts and the Σp of its
+// CTAs in rank order into the tile's histogram and Σp row, and every pick gets its place among the
+// tile's picks of the same expert (unit order), which the dispatch turns into a packed row.
 //
-// One CTA per (128-unit tile, K slice); 128 threads: warp 0 lane 0 issues TMA loads (x tile
-// 128 x 64 and W_gᵀ tile N x 64, 128-byte swizzle) into a ring of stages; warp 1 allocates TMEM
-// and lane 0 issues tcgen05.mma (M = 128, N, K = 16); when the slice is done all four warps
-// read their TMEM lane quarter (one unit per thread) and store the fp32 partial logits. When
-// there are fewer 128-unit tiles than SMs, the reduction dimension is split so that the x stream
-// is spread over about all SMs.
+// Threads: 256. Warp 0 lane 0 issues the TMA loads into a ring of stages, warp 1 owns TMEM and its
+// lane 0 issues the MMAs; all eight warps read TMEM (warp w: lanes 32·(w%4), columns by w/4) and
+// route. Every mbarrier wait is bounded; every CTA of a cluster passes the same cluster barriers
+// whatever happens, so a timeout (status bit set) never leaves a peer waiting.
 #include "moe_device.cuh"
 #include "moe_internal.h"
+#include "select_tile.cuh"
 
 namespace moe {
 
-constexpr int kRtBM = 128, kRtBK = 64, kRtThreads = 128, kRtMaxStages = 8;
-constexpr size_t kRtSmemBudget = 100 * 1024;  // two CTAs per SM
+namespace {
 
-struct RouterTcParams {
+constexpr int kRtBM = 128, kRtBK = 64, kRtThreads = 256, kRtMaxStages = 4;
+constexpr int kRtABytes = kRtBM * kRtBK * 2;       // 16 KB x tile
+constexpr int kRtWBox = 64 * kRtBK * 2;            // 8 KB: 64 experts x 64 rows of W_g
+constexpr int kRtStageBudget = 96 * 1024;          // two CTAs per SM
+constexpr int kRtLdp = 68;                         // row stride (floats) of the partial tile
+
+struct RouteTcParams {
   int64_t Tu;
-  int E, N;
-  int nkb;           // k-blocks in total
-  int kb_per_split;  // k-blocks per slice
-  float* part;       // [S][Tu][E]
-  int64_t part_stride;
+  int E, Np, nblk;       // experts; MMA N = 64·nblk
+  int nkb, kbs;          // k-blocks in total; per cluster rank
+  int S;                 // CTAs per cluster
   int stages;
   uint32_t stage_bytes;
+  const float* logit_bias;
+  float* logits_out;     // [T'][E] or null
+  SelectCtx sel;
+  int32_t* rank_out;     // [T'][K] place of each pick among its tile's picks of the same expert
+  int32_t* tile_hist;    // [tiles][E]
+  float* tile_psum;      // [tiles][E]
   uint32_t* status;
 };
 
+// Shared-memory plan of the epilogue (byte offsets from the 1024-aligned base; the pipeline ring
+// uses the same memory before it).
+struct RtEpi {
+  int R;          // units per CTA
+  int ldl;        // row stride of the logit tile
+  size_t lg, picks, rank, lanes, wpre, gscr, psum, hist, scratch, prefix, total;
+};
+
+__host__ __device__ inline size_t rt_align(size_t n) { return (n + 15) / 16 * 16; }
+
+__host__ __device__ inline RtEpi rt_epi(int S, int E, int epl) {
+  RtEpi L;
+  L.R = kRtBM / S;
+  L.ldl = E + 1;
+  size_t off = rt_align((size_t)kRtBM * kRtLdp * 4);  // the partial tile P first
+  auto take = [&](size_t bytes) { const size_t at = off; off = rt_align(off + bytes); return at; };
+  L.lg = take((size_t)L.R * L.ldl * 4);
+  L.picks = take((size_t)L.R * kPickStride * 4);
+  L.rank = take((size_t)L.R * kPickStride * 4);
+  L.lanes = take((size_t)(kRtThreads / 32) * E * 4);
+  L.wpre = take((size_t)(kRtThreads / 32) * E * 4);
+  L.gscr = take(epl > 0 ? (size_t)(kRtThreads / 32) * 32 * epl * 8 : 0);
+  L.psum = take((size_t)E * 4);
+  L.hist = take((size_t)E * 4);
+  L.scratch = take((size_t)kRtThreads * 4);
+  L.prefix = take((size_t)E * 4);
+  L.total = off;
+  return L;
+}
+
+template <int EPL, int KMAX, bool SIGMOID>
 __global__ void __launch_bounds__(kRtThreads, 1)
-router_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                      RouterTcParams p) {
+route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, RouteTcParams p) {
   extern __shared__ unsigned char smem_dyn[];
   __shared__ __align__(8) uint64_t s_bar[2 * kRtMaxStages + 1];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const uint32_t sbase = (smem_addr(smem_dyn) + 1023u) & ~1023u;
+  unsigned char* gbase = smem_dyn + (sbase - smem_addr(smem_dyn));
   const uint32_t bar0 = smem_addr(s_bar);
-  const int S = p.stages;
+  const int S = p.S, NS = p.stages;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
-  const uint32_t done_bar = bar0 + 8u * (2 * S);
-  const uint32_t tmem_cols = p.N <= 32 ? 32u : (p.N <= 64 ? 64u : (p.N <= 128 ? 128u : 256u));
+  auto empty_bar = [&](int s) { return bar0 + 8u * (NS + s); };
+  const uint32_t done_bar = bar0 + 8u * (2 * NS);
+  const uint32_t tmem_cols = p.Np <= 64 ? 64u : (p.Np <= 128 ? 128u : 256u);
 
-  const int m0 = blockIdx.x * kRtBM;
-  const int kb0 = blockIdx.y * p.kb_per_split;
-  const int kb1 = min(p.nkb, kb0 + p.kb_per_split);
-  const int nk = kb1 - kb0;
+  const int r = S > 1 ? (int)cluster_ctarank() : 0;
+  const int tile = blockIdx.x / S;
+  const int kb0 = r * p.kbs;
+  const int nk = max(0, min(p.nkb, kb0 + p.kbs) - kb0);
 
   if (warp == 0 && lane == 0) {
     s_abort = 0;
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
@@ -71,27 +120,30 @@ router_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
   }
   __syncthreads();
   tc_fence_after();
+  griddep_launch_dependents();
+  griddep_wait();  // x and W_g may come from the previous kernel of the stream
   const uint32_t tmem = s_tmem;
   volatile int* abort_flag = &s_abort;
-  const uint32_t idesc = idesc_bf16_f32(kRtBM, p.N);
+  const uint32_t idesc = idesc_bf16_f32(kRtBM, p.Np) | kIdescBMajorMN;
 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t filled = 0, last_parity = 0;
       for (int i = 0; i < nk; ++i) {
-        const int st = i % S;
-        const uint32_t ph = (uint32_t)(i / S) & 1u;
+        const int st = i % NS;
+        const uint32_t ph = (uint32_t)(i / NS) & 1u;
         if (!mbar_wait(empty_bar(st), ph ^ 1u, abort_flag)) {
           s_abort = 1;
           set_status(p.status, kDevErrTimeout);
-          for (int s = 0; s < S; ++s)
+          for (int s = 0; s < NS; ++s)
             if ((filled >> s) & 1u) mbar_wait(full_bar(s), (last_parity >> s) & 1u, nullptr, 50000000ull);
           break;
         }
         const uint32_t sa = sbase + (uint32_t)st * p.stage_bytes;
+        const int k = (kb0 + i) * kRtBK;
         mbar_arrive_expect_tx(full_bar(st), p.stage_bytes);
-        tma_load_2d(sa, &tmX, full_bar(st), (kb0 + i) * kRtBK, m0);
-        tma_load_2d(sa + kRtBM * kRtBK * 2, &tmW, full_bar(st), (kb0 + i) * kRtBK, 0);
+        tma_load_2d(sa, &tmX, full_bar(st), k, tile * kRtBM);
+        for (int j = 0; j < p.nblk; ++j) tma_load_2d(sa + kRtABytes + j * kRtWBox, &tmW, full_bar(st), 64 * j, k);
         filled |= 1u << st;
         last_parity = (last_parity & ~(1u << st)) | (ph << st);
       }
@@ -101,149 +153,270 @@ router_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
     if (lane == 0) {
       bool aborted = false;
       for (int i = 0; i < nk; ++i) {
-        const int st = i % S;
-        const uint32_t ph = (uint32_t)(i / S) & 1u;
+        const int st = i % NS;
+        const uint32_t ph = (uint32_t)(i / NS) & 1u;
         if (!mbar_wait(full_bar(st), ph, abort_flag)) {
           aborted = true;
           break;
         }
         tc_fence_after();
         const uint32_t sa = sbase + (uint32_t)st * p.stage_bytes;
-        const uint64_t ad = sdesc_kmajor_sw128(sa), bd = sdesc_kmajor_sw128(sa + kRtBM * kRtBK * 2);
+        const uint64_t ad = sdesc_kmajor_sw128(sa);
 #pragma unroll
         for (int k = 0; k < kRtBK / 16; ++k)
-          umma_bf16(tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc, (i > 0 || k > 0) ? 1u : 0u);
+          umma_bf16(tmem, ad + (uint64_t)(2 * k), sdesc_mnmajor_sw128(sa + kRtABytes + k * 2048, kRtWBox), idesc,
+                    (i > 0 || k > 0) ? 1u : 0u);
         umma_commit(empty_bar(st));
       }
       if (aborted) {
         s_abort = 1;
         set_status(p.status, kDevErrTimeout);
       }
-      umma_commit(done_bar);  // also covers the no-work case: arrives once prior MMAs finish
+      umma_commit(done_bar);  // also covers nk == 0: arrives once the earlier MMAs (none) complete
     }
     __syncwarp();
   }
 
-  // epilogue: every warp reads its 32 TMEM lanes = 32 units of the tile
   const bool ok = mbar_wait(done_bar, 0, abort_flag);
-  if (!ok && lane == 0) {
-    s_abort = 1;
-    set_status(p.status, kDevErrTimeout);
-  }
+  if (!ok && tid == 0) set_status(p.status, kDevErrTimeout);
   tc_fence_after();
-  const int64_t u = (int64_t)m0 + warp * 32 + lane;
-  const bool row_ok = ok && nk > 0 && u < p.Tu;
-  float* out = p.part + (int64_t)blockIdx.y * p.part_stride + u * p.E;
-  const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
-  if (ok) {
-    if (p.N == 16) {
-      uint32_t v[16];
-      tmem_ld_32x32b_x16(t_row, v);
-      tmem_ld_wait();
-      if (row_ok) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (j < p.E) out[j] = __uint_as_float(v[j]);
-      }
-    } else {
-      for (int c = 0; c < p.N; c += 32) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(t_row + c, v);
+
+  // ------------------------------------------------------------ logits: partials → my units
+  const RtEpi L = rt_epi(S, p.E, EPL);
+  float* P = reinterpret_cast<float*>(gbase);
+  float* lg = reinterpret_cast<float*>(gbase + L.lg);
+  const int R = L.R, ldl = L.ldl, E = p.E;
+  const int row0 = r * R;
+  const int64_t u0 = (int64_t)tile * kRtBM + row0;
+  const int Rv = (int)max((int64_t)0, min((int64_t)R, p.Tu - u0));
+  const uint32_t p_sh = smem_addr(P);
+  const int npass = p.Np / 64;
+  for (int pass = 0; pass < npass; ++pass) {
+    {
+      const int q4 = warp & 3, half = warp >> 2;  // TMEM lanes 32·q4.., columns 32·half.. of the pass
+      const int row = 32 * q4 + lane;
+      uint32_t v[32];
+      if (ok && nk > 0) {
+        tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(64 * pass + 32 * half), v);
         tmem_ld_wait();
-        if (row_ok) {
-          if ((p.E & 3) == 0 && c + 32 <= p.E) {
-            float4* o4 = reinterpret_cast<float4*>(out + c);
+      } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              o4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-          } else {
+        for (int j = 0; j < 32; ++j) v[j] = 0u;
+      }
+      float4* dst = reinterpret_cast<float4*>(P + row * kRtLdp + 32 * half);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (c + j < p.E) out[c + j] = __uint_as_float(v[j]);
-          }
+      for (int j = 0; j < 8; ++j)
+        dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
+                             __uint_as_float(v[4 * j + 3]));
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (S > 1) cluster_sync_all();  // every peer's partial is in its shared memory
+    // 4 columns per thread: all S partial loads are issued before the first add (the adds run in
+    // rank order)
+    for (int i = tid; i < R * 16; i += kRtThreads) {
+      const int rr = i >> 4, c4 = (i & 15) * 4, e0 = 64 * pass + c4;
+      if (e0 >= E) continue;
+      const int prow = row0 + rr;
+      const uint32_t off = (uint32_t)((prow * kRtLdp + c4) * 4);
+      float4 part[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < S)
+          part[q] = (q == r) ? *reinterpret_cast<const float4*>(P + prow * kRtLdp + c4)
+                             : ld_shared_cluster_v4f32(mapa_shared(p_sh + off, (uint32_t)q));
+      float v[4] = {part[0].x, part[0].y, part[0].z, part[0].w};
+#pragma unroll
+      for (int q = 1; q < 8; ++q)
+        if (q < S) {
+          v[0] += part[q].x; v[1] += part[q].y; v[2] += part[q].z; v[3] += part[q].w;
         }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = e0 + j;
+        if (e >= E) break;
+        float w = v[j];
+        if (p.logit_bias) w = w + p.logit_bias[e];
+        lg[rr * ldl + e] = w;
+        if (p.logits_out && rr < Rv) p.logits_out[(u0 + rr) * E + e] = w;
       }
     }
+    if (S > 1) cluster_sync_all();  // peers are done reading this pass's partial
+    else __syncthreads();
   }
-  tc_fence_before();
-  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, tmem_cols);
   }
-}
 
-// W_gᵀ[n][k] = W_g[k][n] for n < E, 0 for E <= n < N.  (32 x 32 tiles through shared memory)
-__global__ void __launch_bounds__(256)
-router_transpose_kernel(const __nv_bfloat16* __restrict__ w, int hu, int E, int N,
-                        __nv_bfloat16* __restrict__ wt) {
-  __shared__ __nv_bfloat16 tile[32][33];
-  const int k0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  for (int r = ty; r < 32; r += 8) {
-    const int k = k0 + r, n = n0 + tx;
-    tile[r][tx] = (k < hu && n < E) ? w[(int64_t)k * E + n] : __float2bfloat16(0.f);
+  // ------------------------------------------------------------ routing of my units
+  int* picks = reinterpret_cast<int*>(gbase + L.picks);
+  int* rank = reinterpret_cast<int*>(gbase + L.rank);
+  float* psum_s = reinterpret_cast<float*>(gbase + L.psum);
+  int* hist_s = reinterpret_cast<int*>(gbase + L.hist);
+  int* prefix = reinterpret_cast<int*>(gbase + L.prefix);
+  if constexpr (EPL == 0)
+    select_rows_thread<KMAX, SIGMOID>(p.sel, lg, ldl, Rv, u0, picks);
+  else
+    select_rows_warp<EPL, SIGMOID>(p.sel, lg, ldl, Rv, u0, picks, gbase + L.gscr);
+  __syncthreads();
+  column_sums(lg, ldl, Rv, E, psum_s, reinterpret_cast<float*>(gbase + L.scratch));
+  rank_picks(picks, Rv, p.sel.K, E, rank, hist_s, reinterpret_cast<uint32_t*>(gbase + L.lanes),
+             reinterpret_cast<int*>(gbase + L.wpre));
+
+  // ------------------------------------------------------------ the tile's counts and Σp
+  if (S > 1) cluster_sync_all();  // every CTA's counts and Σp are in its shared memory
+  const uint32_t hist_sh = smem_addr(hist_s), psum_sh = smem_addr(psum_s);
+  for (int e = tid; e < E; e += kRtThreads) {
+    int h[8];
+    float ps[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < S) {
+        h[q] = (q == r) ? hist_s[e] : ld_shared_cluster_s32(mapa_shared(hist_sh + 4u * e, (uint32_t)q));
+        if (r == 0) ps[q] = (q == 0) ? psum_s[e] : ld_shared_cluster_f32(mapa_shared(psum_sh + 4u * e, (uint32_t)q));
+      }
+    int pre = 0, tot = 0;
+    float psum = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < S) {
+        if (q < r) pre += h[q];
+        tot += h[q];
+        if (r == 0) psum += ps[q];
+      }
+    prefix[e] = pre;
+    if (r == 0) {
+      p.tile_hist[(int64_t)tile * E + e] = tot;
+      p.tile_psum[(int64_t)tile * E + e] = psum;
+    }
   }
   __syncthreads();
-  for (int r = ty; r < 32; r += 8) {
-    const int n = n0 + r, k = k0 + tx;
-    if (n < N && k < hu) wt[(int64_t)n * hu + k] = tile[tx][r];
+  const int K = p.sel.K;
+  for (int i = tid; i < Rv * K; i += kRtThreads) {
+    const int t = i / K, k = i - t * K;
+    const int e = picks[t * kPickStride + k];
+    p.rank_out[(u0 + t) * K + k] = rank[t * kPickStride + k] + prefix[e];
+  }
+  if (S > 1) cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
+}
+
+// Copy of W_g [h'][E] with its rows padded to Ep columns (zeros past E), for E not a multiple of 8
+// or an unaligned W_g: TMA needs 16-byte row strides.
+__global__ void __launch_bounds__(256)
+router_pad_kernel(const __nv_bfloat16* __restrict__ w, int64_t hu, int E, int Ep, __nv_bfloat16* __restrict__ wp) {
+  const int64_t n = hu * Ep;
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
+    const int64_t k = i / Ep;
+    const int e = (int)(i - k * Ep);
+    wp[i] = e < E ? w[k * E + e] : __float2bfloat16(0.f);
   }
 }
 
-RouterPlan router_plan(const Problem& p) {
-  RouterPlan r;
-  r.N = (p.E + 15) / 16 * 16;
-  r.m_tiles = (int)((p.Tu + kRtBM - 1) / kRtBM);
-  r.nkb = (p.hu + kRtBK - 1) / kRtBK;
-  int S = r.m_tiles > 0 ? (int)(kRouterSplitTarget / r.m_tiles) : 1;
-  if (S < 1) S = 1;
-  if (S > 8) S = 8;
-  if (S > r.nkb / 4) S = r.nkb / 4 > 0 ? r.nkb / 4 : 1;
-  r.kb_per_split = (r.nkb + S - 1) / S;
-  r.splits = (r.nkb + r.kb_per_split - 1) / r.kb_per_split;
-  return r;
-}
-
-cudaError_t launch_router_tc(const Problem& p, const void* x, const void* w_router, void* wt, float* part,
-                             uint32_t* status, cudaStream_t s) {
-  const RouterPlan r = router_plan(p);
-  if (p.Tu == 0) return cudaSuccess;
-  dim3 tg((p.hu + 31) / 32, (r.N + 31) / 32);
-  router_transpose_kernel<<<tg, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(w_router), p.hu, p.E, r.N,
-                                             static_cast<__nv_bfloat16*>(wt));
-  note_launch();
-  CUtensorMap mX, mW;
-  if (!encode_tmap_2d_bf16(&mX, x, (uint64_t)p.hu, (uint64_t)p.Tu, kRtBK, kRtBM) ||
-      !encode_tmap_2d_bf16(&mW, wt, (uint64_t)p.hu, (uint64_t)r.N, kRtBK, (uint32_t)r.N))
-    return cudaErrorInvalidValue;
-  RouterTcParams g;
-  g.Tu = p.Tu;
-  g.E = p.E;
-  g.N = r.N;
-  g.nkb = r.nkb;
-  g.kb_per_split = r.kb_per_split;
-  g.part = part;
-  g.part_stride = p.Tu * p.E;
-  g.stage_bytes = (uint32_t)(kRtBM * kRtBK * 2 + r.N * kRtBK * 2);
-  int stages = (int)(kRtSmemBudget / g.stage_bytes);
-  if (stages < 3) stages = 3;
-  g.stages = stages > kRtMaxStages ? kRtMaxStages : stages;
-  g.status = status;
-  const size_t smem = (size_t)g.stages * g.stage_bytes + 1024;
+template <int EPL, int KMAX, bool SIGMOID>
+cudaError_t launch_rt(const CUtensorMap& mX, const CUtensorMap& mW, const RouteTcParams& g, unsigned grid,
+                      size_t smem, cudaStream_t s, bool pdl) {
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(router_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(3 * (kRtBM * kRtBK * 2 + 256 * kRtBK * 2) + 1024));
+    cudaError_t e = cudaFuncSetAttribute(route_tc_kernel<EPL, KMAX, SIGMOID>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kRtStageBudget + 1024));
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  router_gemm_tc_kernel<<<dim3(r.m_tiles, r.splits), kRtThreads, smem, s>>>(mX, mW, g);
-  note_launch();
-  return cudaGetLastError();
+  return launch_kernel(route_tc_kernel<EPL, KMAX, SIGMOID>, dim3(grid), dim3(kRtThreads), smem, s, (unsigned)g.S, pdl,
+                       mX, mW, g);
+}
+
+}  // namespace
+
+RouterPlan router_plan(const Problem& p, int sms) {
+  RouterPlan r;
+  r.nblk = (p.E + 63) / 64;
+  r.Np = 64 * r.nblk;
+  r.m_tiles = (int)((p.Tu + kRtBM - 1) / kRtBM);
+  r.nkb = (p.hu + kRtBK - 1) / kRtBK;
+  // K slices per tile: about two CTAs per SM stream x, each slice at least one k-block; then as
+  // many more as the epilogue's shared memory needs (its logit tile shrinks with 128/S units)
+  const int epl = p.E <= 64 ? 0 : (p.E <= 128 ? 4 : 8);
+  int S = 1;
+  while (S < 8 && (int64_t)r.m_tiles * S * 2 <= 2LL * sms && S * 2 <= r.nkb) S *= 2;
+  while (S < 8 && rt_epi(S, p.E, epl).total > (size_t)kRtStageBudget) S *= 2;
+  r.S = S;
+  r.kbs = (r.nkb + S - 1) / S;
+  return r;
+}
+
+static bool router_needs_pad(const Problem& p, const void* w_router) {
+  return p.E % 8 != 0 || (reinterpret_cast<uintptr_t>(w_router) & 15) != 0;
+}
+
+cudaError_t launch_route_tc(const Problem& p, const void* x, const void* w_router, const float* logit_bias,
+                            const SelectCtx& sel, float* logits_out, int32_t* rank_out, int32_t* tile_hist,
+                            float* tile_psum, void* w_pad, uint32_t* status, cudaStream_t s) {
+  if (p.Tu == 0) return cudaSuccess;
+  const RouterPlan r = router_plan(p, device_sm_count());
+  const void* wsrc = w_router;
+  int Ew = p.E;
+  bool pdl = false;
+  if (router_needs_pad(p, w_router)) {
+    Ew = (p.E + 7) / 8 * 8;
+    const int64_t n = (int64_t)p.hu * Ew;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    cudaError_t e = launch_kernel(router_pad_kernel, dim3((unsigned)blocks), dim3(256), 0, s, 1, false,
+                                  static_cast<const __nv_bfloat16*>(w_router), (int64_t)p.hu, p.E, Ew,
+                                  static_cast<__nv_bfloat16*>(w_pad));
+    if (e != cudaSuccess) return e;
+    wsrc = w_pad;
+    pdl = true;
+  }
+  CUtensorMap mX, mW;
+  if (!encode_tmap_2d_bf16(&mX, x, (uint64_t)p.hu, (uint64_t)p.Tu, kRtBK, kRtBM) ||
+      !encode_tmap_2d_bf16(&mW, wsrc, (uint64_t)Ew, (uint64_t)p.hu, 64, kRtBK))
+    return cudaErrorInvalidValue;
+  RouteTcParams g;
+  g.Tu = p.Tu;
+  g.E = p.E;
+  g.Np = r.Np;
+  g.nblk = r.nblk;
+  g.nkb = r.nkb;
+  g.kbs = r.kbs;
+  g.S = r.S;
+  g.stage_bytes = (uint32_t)(kRtABytes + r.nblk * kRtWBox);
+  int stages = (int)(kRtStageBudget / g.stage_bytes);
+  g.stages = stages < 2 ? 2 : (stages > kRtMaxStages ? kRtMaxStages : stages);
+  g.logit_bias = logit_bias;
+  g.logits_out = logits_out;
+  g.sel = sel;
+  g.rank_out = rank_out;
+  g.tile_hist = tile_hist;
+  g.tile_psum = tile_psum;
+  g.status = status;
+  const bool warp_sel = p.E > 64;
+  const int epl = !warp_sel ? 0 : (p.E <= 128 ? 4 : 8);
+  const RtEpi L = rt_epi(r.S, p.E, epl);
+  size_t smem = (size_t)g.stages * g.stage_bytes;
+  if (L.total > smem) smem = L.total;
+  smem += 1024;
+  if (smem > (size_t)kRtStageBudget + 1024) return cudaErrorInvalidConfiguration;
+  const unsigned grid = (unsigned)(r.m_tiles * r.S);
+  const int kb = p.K <= 2 ? 2 : (p.K <= 4 ? 4 : 8);
+  if (warp_sel) {
+    if (epl == 4) return p.sigmoid ? launch_rt<4, 8, true>(mX, mW, g, grid, smem, s, pdl)
+                                   : launch_rt<4, 8, false>(mX, mW, g, grid, smem, s, pdl);
+    return p.sigmoid ? launch_rt<8, 8, true>(mX, mW, g, grid, smem, s, pdl)
+                     : launch_rt<8, 8, false>(mX, mW, g, grid, smem, s, pdl);
+  }
+  if (p.sigmoid) {
+    if (kb == 2) return launch_rt<0, 2, true>(mX, mW, g, grid, smem, s, pdl);
+    if (kb == 4) return launch_rt<0, 4, true>(mX, mW, g, grid, smem, s, pdl);
+    return launch_rt<0, 8, true>(mX, mW, g, grid, smem, s, pdl);
+  }
+  if (kb == 2) return launch_rt<0, 2, false>(mX, mW, g, grid, smem, s, pdl);
+  if (kb == 4) return launch_rt<0, 4, false>(mX, mW, g, grid, smem, s, pdl);
+  return launch_rt<0, 8, false>(mX, mW, g, grid, smem, s, pdl);
 }
 
 }  // namespace moe
