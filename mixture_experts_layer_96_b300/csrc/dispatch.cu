@@ -10,7 +10,7 @@
 //   scan:  a block per expert: the exclusive scan of the expert's column of chunk counts gives
 //          each chunk's base in the expert's queue and the pre-drop count; the same block reduces
 //          the expert's Σp column for the aux loss. The last block to finish (ticket) scans the
-//          kept rows n_e = min(count_e, C) into the offsets and adds the aux terms in expert order.
+//          kept rows n_e = min(count_e, C) into the offsets and adds the aux terms (fixed tree).
 //   pack:  one warp per unit: place = chunk base + place in chunk; kept if place < C, at packed row
 //          offsets[e] + place; the unit's x row is read once and written to each of its kept rows.
 // Integer sums only (besides the fixed-order aux sums), no atomics whose order matters, no
@@ -61,29 +61,43 @@ chunk_rank_kernel(const int32_t* __restrict__ idx, int64_t Tu, int K, int E, int
   for (int e = t; e < E; e += kChunk) chunk_hist[(int64_t)blockIdx.x * E + e] = hist[e];
 }
 
+// Σp in fixed point: a tile's Σ_t p_{t,e} (fp32, at most 128) times 2^40 is an exact integer for
+// any value >= 2^-16, and integer sums do not depend on their order, so the per-expert totals are
+// deterministic without a fixed summation tree (and without fp64, which is slow on this GPU).
+constexpr float kPsumScale = 1099511627776.0f;  // 2^40
+
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+  for (int d = 16; d; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  return v;
+}
+
 // One block per expert e:
 //   chunk_base[c][e] = Σ_{c'<c} hist[c'][e]; count_e = Σ_c hist[c][e]   (one chunk per thread per
 //   pass, a block scan per pass)
-//   term_e = (count_e/(T'·K))·(Σ_c psum[c][e] / T')   when psum is given (fp64, fixed order)
+//   term_e = (count_e/(T'·K))·(Σ_c psum[c][e] / T')   when psum is given
 // The last block (ticket): offsets = exclusive scan over experts of min(count_e, C); aux loss =
-// α·E·Σ_e term_e in expert order; the ticket is reset for the next call.
+// α·E·Σ_e term_e (a fixed-order tree over the experts); the ticket is reset for the next call.
 __global__ void __launch_bounds__(kScanThreads)
 scan_kernel(const int32_t* __restrict__ hist, int64_t nchunks, int E, int64_t C, const float* __restrict__ psum,
             int64_t Tu, int K, float alpha, int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts_ws,
-            int32_t* __restrict__ offsets_ws, int32_t* counts_out, int32_t* offsets_out, double* terms,
+            int32_t* __restrict__ offsets_ws, int32_t* counts_out, int32_t* offsets_out, float* terms,
             unsigned int* ticket, float* aux_out) {
   __shared__ int warp_tot[kScanThreads / 32];
+  __shared__ long long warp_p[kScanThreads / 32];
   __shared__ int excl[kMaxExperts + 1];
-  __shared__ double sP[kScanThreads];
+  __shared__ float tv[kMaxExperts];
   __shared__ bool last;
   griddep_launch_dependents();
   griddep_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int e = blockIdx.x;
   int carry = 0;
+  long long pfx = 0;
   for (int64_t c0 = 0; c0 < nchunks; c0 += kScanThreads) {
     const int64_t c = c0 + tid;
     const int v = c < nchunks ? hist[c * E + e] : 0;
+    if (psum && c < nchunks) pfx += __float2ll_rn(psum[c * E + e] * kPsumScale);
     int incl = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -103,19 +117,19 @@ scan_kernel(const int32_t* __restrict__ hist, int64_t nchunks, int E, int64_t C,
     __syncthreads();
   }
   if (psum) {
-    double P = 0.0;
-    for (int64_t c = tid; c < nchunks; c += kScanThreads) P += (double)psum[c * E + e];
-    sP[tid] = P;
+    pfx = warp_sum_ll(pfx);
+    if (lane == 0) warp_p[warp] = pfx;
     __syncthreads();
-    for (int s = kScanThreads / 2; s; s >>= 1) {
-      if (tid < s) sP[tid] += sP[tid + s];
-      __syncthreads();
-    }
   }
   if (tid == 0) {
     counts_ws[e] = carry;
     if (counts_out) counts_out[e] = carry;
-    if (psum) terms[e] = Tu > 0 ? ((double)carry / ((double)Tu * K)) * (sP[0] / (double)Tu) : 0.0;
+    if (psum) {
+      long long P = 0;
+      for (int w = 0; w < kScanThreads / 32; ++w) P += warp_p[w];
+      const float Pe = __ll2float_rn(P) * (1.0f / kPsumScale);
+      terms[e] = Tu > 0 ? ((float)carry / ((float)Tu * (float)K)) * (Pe / (float)Tu) : 0.0f;
+    }
     __threadfence();
     last = atomicAdd(ticket, 1u) == (unsigned)(E - 1);
   }
@@ -148,22 +162,22 @@ scan_kernel(const int32_t* __restrict__ hist, int64_t nchunks, int E, int64_t C,
     if (lane == 31) excl[E] = incl;
   }
   if (psum && aux_out) {
-    const volatile double* vt = terms;
-    for (int i = tid; i < E; i += kScanThreads) sP[i] = vt[i];
+    const volatile float* vt = terms;
+    for (int i = tid; i < kMaxExperts; i += kScanThreads) tv[i] = i < E ? vt[i] : 0.0f;
   }
   __syncthreads();
   for (int i = tid; i <= E; i += kScanThreads) {
     offsets_ws[i] = excl[i];
     if (offsets_out) offsets_out[i] = excl[i];
   }
-  if (tid == 0) {
-    if (psum && aux_out) {
-      double acc = 0.0;
-      for (int i = 0; i < E; ++i) acc += sP[i];  // expert order
-      *aux_out = (float)((double)alpha * E * acc);
+  if (psum && aux_out) {  // pairwise tree over the 256 slots (fixed order), then the scale
+    for (int s = kMaxExperts / 2; s; s >>= 1) {
+      if (tid < s) tv[tid] += tv[tid + s];
+      __syncthreads();
     }
-    *ticket = 0u;
+    if (tid == 0) *aux_out = alpha * (float)E * tv[0];
   }
+  if (tid == 0) *ticket = 0u;
 }
 
 // One warp per unit: slots of its picks, then its x row (row_vecs 16-byte vectors) copied to each
@@ -253,7 +267,7 @@ pack_bytes_kernel(const unsigned char* __restrict__ x, const int32_t* __restrict
 
 cudaError_t launch_scan(const Problem& p, int64_t nchunks, const int32_t* hist, const float* psum,
                         int32_t* chunk_base, int32_t* counts_ws, int32_t* offsets_ws, int32_t* counts_out,
-                        int32_t* offsets_out, double* terms, unsigned int* ticket, float* aux_out, cudaStream_t s,
+                        int32_t* offsets_out, float* terms, unsigned int* ticket, float* aux_out, cudaStream_t s,
                         bool pdl) {
   return launch_kernel(scan_kernel, dim3((unsigned)p.E), dim3(kScanThreads), 0, s, 1, pdl, hist, nchunks, p.E, p.C,
                        psum, p.Tu, p.K, p.cfg.aux_alpha, chunk_base, counts_ws, offsets_ws, counts_out, offsets_out,

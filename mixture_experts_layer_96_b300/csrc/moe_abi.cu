@@ -135,7 +135,7 @@ WsLayout ws_layout(const Problem& p) {
   L.chunk_hist = take((size_t)p.ntiles * E * 4);
   L.chunk_base = take((size_t)p.ntiles * E * 4);
   L.psum = take((size_t)p.ntiles * E * 4);
-  L.aux_terms = take(E * 8);
+  L.aux_terms = take(E * 4);
   L.w_pad = take(p.bf16 ? (size_t)p.hu * ((E + 7) / 8 * 8) * 2 : 0);
   L.logits = take(p.bf16 ? 0 : (size_t)p.Tu * E * 4);
   L.rank = take(TK * 4);
@@ -274,7 +274,7 @@ static cudaError_t scan_stage(const Problem& p, void* ws, int32_t* counts_out, i
   const WsLayout L = ws_layout(p);
   return launch_scan(p, p.ntiles, ws_ptr<int32_t>(ws, L.chunk_hist), aux_out ? ws_ptr<float>(ws, L.psum) : nullptr,
                      ws_ptr<int32_t>(ws, L.chunk_base), ws_ptr<int32_t>(ws, L.counts), ws_ptr<int32_t>(ws, L.offsets),
-                     counts_out, offsets_out, ws_ptr<double>(ws, L.aux_terms),
+                     counts_out, offsets_out, ws_ptr<float>(ws, L.aux_terms),
                      ws_ptr<unsigned int>(ws, L.status + 8), aux_out, s, true);
 }
 

@@ -59,7 +59,7 @@ struct WsLayout {
   size_t chunk_hist;   // int32 [ntiles][E] picks per expert of each tile / chunk
   size_t chunk_base;   // int32 [ntiles][E] each tile's / chunk's base in the expert queues
   size_t psum;         // float [ntiles][E] Σ over the tile's units of p_{t,e}
-  size_t aux_terms;    // double [E] per-expert aux terms
+  size_t aux_terms;    // float [E] per-expert aux terms
   size_t w_pad;        // bf16 [h'][E rounded up to 8] router weight copy (bf16 layers, when needed)
   size_t logits;       // float [T'][E] router logits (fp32 layers)
   size_t rank;         // int32 [T'][K] pick places within their tile (routing calls alone)
@@ -162,7 +162,7 @@ cudaError_t launch_select_logits(const Problem& p, const float* logits, const fl
 // Per expert: chunk bases, pre-drop counts, offsets; the aux loss when psum and aux_out are given.
 cudaError_t launch_scan(const Problem& p, int64_t nchunks, const int32_t* hist, const float* psum,
                         int32_t* chunk_base, int32_t* counts_ws, int32_t* offsets_ws, int32_t* counts_out,
-                        int32_t* offsets_out, double* terms, unsigned int* ticket, float* aux_out, cudaStream_t s,
+                        int32_t* offsets_out, float* terms, unsigned int* ticket, float* aux_out, cudaStream_t s,
                         bool pdl);
 // Slots of the picks (slot_of holds the places within chunks of 2^chunk_shift units on entry) and
 // the packed rows.

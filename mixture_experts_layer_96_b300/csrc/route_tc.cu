@@ -32,8 +32,8 @@ namespace {
 constexpr int kRtBM = 128, kRtBK = 64, kRtThreads = 256, kRtMaxStages = 4;
 constexpr int kRtABytes = kRtBM * kRtBK * 2;       // 16 KB x tile
 constexpr int kRtWBox = 64 * kRtBK * 2;            // 8 KB: 64 experts x 64 rows of W_g
-constexpr int kRtStageBudget = 96 * 1024;          // two CTAs per SM
-constexpr int kRtLdp = 68;                         // row stride (floats) of the partial tile
+constexpr int kRtStageBudget = 110 * 1024;         // ring or epilogue: two CTAs per SM
+constexpr int kRtFastBudget = 110 * 1024;          // ring + fast epilogue, two CTAs per SM
 
 struct RouteTcParams {
   int64_t Tu;
@@ -42,6 +42,7 @@ struct RouteTcParams {
   int S;                 // CTAs per cluster
   int stages;
   uint32_t stage_bytes;
+  uint32_t epi_off;      // fast epilogue: its shared memory starts here (past the stage ring)
   const float* logit_bias;
   float* logits_out;     // [T'][E] or null
   SelectCtx sel;
@@ -56,22 +57,28 @@ struct RouteTcParams {
 struct RtEpi {
   int R;          // units per CTA
   int ldl;        // row stride of the logit tile
+  int cw, ldp;    // columns per reduction pass; row stride (floats) of the partial tile
   size_t lg, picks, rank, lanes, wpre, gscr, psum, hist, scratch, prefix, total;
 };
 
 __host__ __device__ inline size_t rt_align(size_t n) { return (n + 15) / 16 * 16; }
 
+// Reduction passes of 128 columns when a cluster adds partials of at least 128 experts (half the
+// cluster barriers of 64-column passes), else 64.
 __host__ __device__ inline RtEpi rt_epi(int S, int E, int epl) {
   RtEpi L;
   L.R = kRtBM / S;
   L.ldl = E + 1;
-  size_t off = rt_align((size_t)kRtBM * kRtLdp * 4);  // the partial tile P first
+  L.cw = (S > 1 && E > 64) ? 128 : 64;
+  L.ldp = L.cw + 4;
+  size_t off = rt_align((size_t)kRtBM * L.ldp * 4);  // the partial tile P first
   auto take = [&](size_t bytes) { const size_t at = off; off = rt_align(off + bytes); return at; };
+  const int rw = (L.R + 31) / 32;  // warps holding rows
   L.lg = take((size_t)L.R * L.ldl * 4);
   L.picks = take((size_t)L.R * kPickStride * 4);
   L.rank = take((size_t)L.R * kPickStride * 4);
-  L.lanes = take((size_t)(kRtThreads / 32) * E * 4);
-  L.wpre = take((size_t)(kRtThreads / 32) * E * 4);
+  L.lanes = take((size_t)rw * E * 4);
+  L.wpre = take((size_t)rw * E * 4);
   L.gscr = take(epl > 0 ? (size_t)(kRtThreads / 32) * 32 * epl * 8 : 0);
   L.psum = take((size_t)E * 4);
   L.hist = take((size_t)E * 4);
@@ -81,8 +88,63 @@ __host__ __device__ inline RtEpi rt_epi(int S, int E, int epl) {
   return L;
 }
 
-template <int EPL, int KMAX, bool SIGMOID>
-__global__ void __launch_bounds__(kRtThreads, 1)
+// Shared memory of the fast epilogue (softmax, no group limit, E <= 64), placed past the stage ring:
+// peers push into recv_* while this CTA may still be in its main loop.
+struct RtFast {
+  int R, ec;      // units per CTA; E rounded up to 4
+  int ldr;        // row stride (floats) of the receive buffer: ec + 4, so a warp's 16-byte row
+                  // writes and reads spread over all banks
+  size_t recv_l, recv_h, recv_p, picks, rank, lanes, wpre, wpsum, psum, hist, total;
+};
+
+__host__ __device__ inline RtFast rt_fast(int S, int E) {
+  RtFast L;
+  L.R = kRtBM / S;
+  L.ec = (E + 3) / 4 * 4;
+  L.ldr = L.ec + 4;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { const size_t at = off; off = rt_align(off + bytes); return at; };
+  const bool cl = S > 1;
+  L.recv_l = take(cl ? (size_t)S * L.R * L.ldr * 4 : 0);
+  L.recv_h = take(cl ? (size_t)S * E * 4 : 0);
+  L.recv_p = take(cl ? (size_t)S * E * 4 : 0);
+  L.picks = take((size_t)L.R * kPickStride * 4);
+  L.rank = take((size_t)L.R * kPickStride * 4);
+  L.lanes = take((size_t)(kRtThreads / 32) * E * 4);
+  L.wpre = take((size_t)(kRtThreads / 32) * E * 4);
+  L.wpsum = take((size_t)4 * E * 4);
+  L.psum = take((size_t)E * 4);
+  L.hist = take((size_t)E * 4);
+  L.total = off;
+  return L;
+}
+
+// One TMEM row (this thread's lane) of EM fp32 columns into registers.
+template <int EM>
+__device__ __forceinline__ void tmem_row(uint32_t taddr, float (&v)[EM]) {
+  if constexpr (EM <= 16) {
+    uint32_t r[16];
+    tmem_ld_32x32b_x16(taddr, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < EM; ++j) v[j] = __uint_as_float(r[j]);
+  } else {
+#pragma unroll
+    for (int c = 0; c < EM; c += 32) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[c + j] = __uint_as_float(r[j]);
+    }
+  }
+}
+
+// Threads per CTA: the fast epilogue routes one unit per thread of warps 0-3, so it runs 128.
+__host__ __device__ constexpr int rt_threads(int fem) { return fem > 0 ? 128 : kRtThreads; }
+
+template <int EPL, int KMAX, bool SIGMOID, int FEM>
+__global__ void __launch_bounds__(rt_threads(FEM), 1)
 route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, RouteTcParams p) {
   extern __shared__ unsigned char smem_dyn[];
   __shared__ __align__(8) uint64_t s_bar[2 * kRtMaxStages + 1];
@@ -120,6 +182,10 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
   }
   __syncthreads();
   tc_fence_after();
+  // fast epilogue: peers write into this CTA's shared memory, which is only valid once every CTA of
+  // the cluster runs; the matching wait comes before the first such write
+  if constexpr (FEM > 0)
+    if (S > 1) cluster_arrive_relaxed();
   griddep_launch_dependents();
   griddep_wait();  // x and W_g may come from the previous kernel of the stream
   const uint32_t tmem = s_tmem;
@@ -181,6 +247,173 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
   if (!ok && tid == 0) set_status(p.status, kDevErrTimeout);
   tc_fence_after();
 
+  if constexpr (FEM > 0) {
+    constexpr int NT = rt_threads(FEM);
+    // ---------------------------------------------------------- fast epilogue (registers)
+    const RtFast F = rt_fast(S, p.E);
+    unsigned char* fb = gbase + p.epi_off;
+    const uint32_t fb_sh = sbase + p.epi_off;
+    const int R = F.R, E = p.E, K = p.sel.K;
+    const int row0 = r * R;
+    const int64_t u0 = (int64_t)tile * kRtBM + row0;
+    const int Rv = (int)max((int64_t)0, min((int64_t)R, p.Tu - u0));
+    float l[FEM];
+    if (S > 1) cluster_wait();  // every CTA of the cluster has started
+    // 1. this CTA's partial logits of TMEM row `row` (warps 0-3: one row per thread)
+    if (warp < 4) {
+      const int row = 32 * warp + lane;
+      if (ok && nk > 0) tmem_row<FEM>(tmem + ((uint32_t)(32 * warp) << 16), l);
+      else {
+#pragma unroll
+        for (int e = 0; e < FEM; ++e) l[e] = 0.f;
+      }
+      if (S > 1) {
+        // push the row to the CTA that routes it: slice r of its receive buffer
+        const int q = row / R, rr = row - q * R;
+        const uint32_t dst = mapa_shared(fb_sh + (uint32_t)(F.recv_l + ((size_t)(r * R + rr) * F.ldr) * 4), (uint32_t)q);
+#pragma unroll
+        for (int e = 0; e < FEM; e += 4)
+          if (e < F.ec) st_shared_cluster_v4f32(dst + 4u * e, l[e], l[e + 1], l[e + 2], l[e + 3]);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, tmem_cols);
+    }
+    if (S > 1) {
+      cluster_sync_all();  // every slice of my units is in my receive buffer
+      if (tid < R) {
+        const float* rl = reinterpret_cast<const float*>(fb + F.recv_l);
+#pragma unroll
+        for (int e = 0; e < FEM; e += 4) {
+          if (e >= F.ec) break;
+          const float4 a = *reinterpret_cast<const float4*>(rl + (size_t)tid * F.ldr + e);
+          l[e] = a.x; l[e + 1] = a.y; l[e + 2] = a.z; l[e + 3] = a.w;
+        }
+        for (int q = 1; q < S; ++q)
+#pragma unroll
+          for (int e = 0; e < FEM; e += 4) {
+            if (e >= F.ec) break;
+            const float4 a = *reinterpret_cast<const float4*>(rl + ((size_t)q * R + tid) * F.ldr + e);
+            l[e] += a.x; l[e + 1] += a.y; l[e + 2] += a.z; l[e + 3] += a.w;
+          }
+      }
+    }
+    // 2. route my units: thread t < Rv routes unit u0 + t
+    uint32_t* wcount = reinterpret_cast<uint32_t*>(fb + F.lanes);  // [4 warps][E] picks per expert
+    float* wpsum = reinterpret_cast<float*>(fb + F.wpsum);
+    float* psum_s = reinterpret_cast<float*>(fb + F.psum);
+    int* hist_s = reinterpret_cast<int*>(fb + F.hist);
+    float pr[FEM];
+    int pk[KMAX], rk[KMAX];
+#pragma unroll
+    for (int e = 0; e < FEM; ++e) pr[e] = 0.f;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) { pk[k] = -1; rk[k] = 0; }
+    if (tid < Rv) {
+#pragma unroll
+      for (int e = 0; e < FEM; ++e)
+        if (e < E && p.logit_bias) l[e] = l[e] + p.logit_bias[e];
+      const int64_t u = u0 + tid;
+      if (p.logits_out) {
+#pragma unroll
+        for (int e = 0; e < FEM; ++e)
+          if (e < E) p.logits_out[u * E + e] = l[e];
+      }
+      float gv[KMAX];
+      route_unit_regs<FEM, KMAX>(l, E, K, pk, gv, pr);
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if (k < K) {
+          p.sel.idx[u * K + k] = pk[k];
+          p.sel.gate[u * K + k] = gv[k];
+        }
+    }
+    // 3. Σ_t p[t][e] over my units (warp reduce-scatter, then the warps in order), and the picks per
+    // expert of each warp with each pick's place among them (a ballot per expert)
+    const uint32_t lt = lanemask_lt();
+    if (warp < 4) {
+      warp_reduce_scatter<FEM>(pr, lane);
+      if constexpr (FEM >= 32) {
+#pragma unroll
+        for (int j = 0; j < FEM / 32; ++j) {
+          const int e = lane * (FEM / 32) + j;
+          if (e < E) wpsum[warp * E + e] = pr[j];
+        }
+      } else {
+        const int g = 32 / FEM;
+        if ((lane % g) == 0 && lane / g < E) wpsum[warp * E + lane / g] = pr[0];
+      }
+      for (int e = 0; e < E; ++e) {
+        bool mine = false;
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) mine |= pk[k] == e;
+        const uint32_t m = __ballot_sync(0xffffffffu, mine);
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+          if (pk[k] == e) rk[k] = __popc(m & lt);
+        if (lane == 0) wcount[warp * E + e] = (uint32_t)__popc(m);
+      }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += NT) {
+      psum_s[e] = ((wpsum[e] + wpsum[E + e]) + wpsum[2 * E + e]) + wpsum[3 * E + e];
+      hist_s[e] = (int)(wcount[e] + wcount[E + e] + wcount[2 * E + e] + wcount[3 * E + e]);
+    }
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      if (pk[k] >= 0)
+        for (int w = 0; w < warp; ++w) rk[k] += (int)wcount[w * E + pk[k]];
+    __syncthreads();
+    // 4. the tile's counts and Σp; each pick's place in the tile
+    if (S == 1) {
+      for (int e = tid; e < E; e += NT) {
+        p.tile_hist[(int64_t)tile * E + e] = hist_s[e];
+        p.tile_psum[(int64_t)tile * E + e] = psum_s[e];
+      }
+      if (tid < Rv)
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+          if (k < K) p.rank_out[(u0 + tid) * K + k] = rk[k];
+    } else {
+      // push my counts to every CTA (prefixes) and my Σp to rank 0 (tile totals)
+      for (int i = tid; i < S * E; i += NT) {
+        const int q = i / E, e = i - q * E;
+        st_shared_cluster_u32(mapa_shared(fb_sh + (uint32_t)(F.recv_h + ((size_t)r * E + e) * 4), (uint32_t)q),
+                              (uint32_t)hist_s[e]);
+        if (q == 0)
+          st_shared_cluster_f32(mapa_shared(fb_sh + (uint32_t)(F.recv_p + ((size_t)r * E + e) * 4), 0u), psum_s[e]);
+      }
+      cluster_sync_all();  // every CTA's counts (and Σp at rank 0) have arrived; no remote access follows
+      const int* rh = reinterpret_cast<const int*>(fb + F.recv_h);
+      const float* rp = reinterpret_cast<const float*>(fb + F.recv_p);
+      int* prefix = reinterpret_cast<int*>(fb + F.wpre);
+      for (int e = tid; e < E; e += NT) {
+        int pre = 0, tot = 0;
+        float ps = 0.f;
+        for (int q = 0; q < S; ++q) {
+          const int h = rh[q * E + e];
+          if (q < r) pre += h;
+          tot += h;
+          if (r == 0) ps += rp[q * E + e];
+        }
+        prefix[e] = pre;
+        if (r == 0) {
+          p.tile_hist[(int64_t)tile * E + e] = tot;
+          p.tile_psum[(int64_t)tile * E + e] = ps;
+        }
+      }
+      __syncthreads();
+      if (tid < Rv)
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+          if (k < K) p.rank_out[(u0 + tid) * K + k] = rk[k] + prefix[pk[k]];
+    }
+    return;
+  }
+
   // ------------------------------------------------------------ logits: partials → my units
   const RtEpi L = rt_epi(S, p.E, EPL);
   float* P = reinterpret_cast<float*>(gbase);
@@ -190,40 +423,45 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
   const int64_t u0 = (int64_t)tile * kRtBM + row0;
   const int Rv = (int)max((int64_t)0, min((int64_t)R, p.Tu - u0));
   const uint32_t p_sh = smem_addr(P);
-  const int npass = p.Np / 64;
+  const int cw = L.cw, ldp = L.ldp;
+  const int npass = p.Np / cw;
   for (int pass = 0; pass < npass; ++pass) {
     {
-      const int q4 = warp & 3, half = warp >> 2;  // TMEM lanes 32·q4.., columns 32·half.. of the pass
+      // warp w: TMEM lanes 32·(w%4) (its rows), columns cw/2·(w/4) .. of the pass
+      const int q4 = warp & 3, half = warp >> 2;
       const int row = 32 * q4 + lane;
-      uint32_t v[32];
-      if (ok && nk > 0) {
-        tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(64 * pass + 32 * half), v);
-        tmem_ld_wait();
-      } else {
+      for (int c0 = 0; c0 < cw / 2; c0 += 32) {
+        uint32_t v[32];
+        if (ok && nk > 0) {
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(cw * pass + (cw / 2) * half + c0), v);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = 0u;
+          for (int j = 0; j < 32; ++j) v[j] = 0u;
+        }
+        float4* dst = reinterpret_cast<float4*>(P + row * ldp + (cw / 2) * half + c0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
+                               __uint_as_float(v[4 * j + 3]));
       }
-      float4* dst = reinterpret_cast<float4*>(P + row * kRtLdp + 32 * half);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
-                             __uint_as_float(v[4 * j + 3]));
     }
     tc_fence_before();
     __syncthreads();
     if (S > 1) cluster_sync_all();  // every peer's partial is in its shared memory
     // 4 columns per thread: all S partial loads are issued before the first add (the adds run in
     // rank order)
-    for (int i = tid; i < R * 16; i += kRtThreads) {
-      const int rr = i >> 4, c4 = (i & 15) * 4, e0 = 64 * pass + c4;
+    const int c4n = cw / 4;
+    for (int i = tid; i < R * c4n; i += kRtThreads) {
+      const int rr = i / c4n, c4 = (i - rr * c4n) * 4, e0 = cw * pass + c4;
       if (e0 >= E) continue;
       const int prow = row0 + rr;
-      const uint32_t off = (uint32_t)((prow * kRtLdp + c4) * 4);
+      const uint32_t off = (uint32_t)((prow * ldp + c4) * 4);
       float4 part[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         if (q < S)
-          part[q] = (q == r) ? *reinterpret_cast<const float4*>(P + prow * kRtLdp + c4)
+          part[q] = (q == r) ? *reinterpret_cast<const float4*>(P + prow * ldp + c4)
                              : ld_shared_cluster_v4f32(mapa_shared(p_sh + off, (uint32_t)q));
       float v[4] = {part[0].x, part[0].y, part[0].z, part[0].w};
 #pragma unroll
@@ -313,20 +551,29 @@ router_pad_kernel(const __nv_bfloat16* __restrict__ w, int64_t hu, int E, int Ep
   }
 }
 
-template <int EPL, int KMAX, bool SIGMOID>
+template <int EPL, int KMAX, bool SIGMOID, int FEM>
 cudaError_t launch_rt(const CUtensorMap& mX, const CUtensorMap& mW, const RouteTcParams& g, unsigned grid,
                       size_t smem, cudaStream_t s, bool pdl) {
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(route_tc_kernel<EPL, KMAX, SIGMOID>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kRtStageBudget + 1024));
+    cudaError_t e = cudaFuncSetAttribute(route_tc_kernel<EPL, KMAX, SIGMOID, FEM>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)((kRtFastBudget > kRtStageBudget ? kRtFastBudget : kRtStageBudget) + 1024));
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  return launch_kernel(route_tc_kernel<EPL, KMAX, SIGMOID>, dim3(grid), dim3(kRtThreads), smem, s, (unsigned)g.S, pdl,
-                       mX, mW, g);
+  return launch_kernel(route_tc_kernel<EPL, KMAX, SIGMOID, FEM>, dim3(grid), dim3(rt_threads(FEM)), smem, s,
+                       (unsigned)g.S, pdl, mX, mW, g);
+}
+
+template <int FEM>
+cudaError_t launch_rt_fast(const CUtensorMap& mX, const CUtensorMap& mW, const RouteTcParams& g, int K, unsigned grid,
+                           size_t smem, cudaStream_t s, bool pdl) {
+  if (K <= 2) return launch_rt<0, 2, false, FEM>(mX, mW, g, grid, smem, s, pdl);
+  if (K <= 4) return launch_rt<0, 4, false, FEM>(mX, mW, g, grid, smem, s, pdl);
+  return launch_rt<0, 8, false, FEM>(mX, mW, g, grid, smem, s, pdl);
 }
 
 }  // namespace
@@ -376,7 +623,7 @@ cudaError_t launch_route_tc(const Problem& p, const void* x, const void* w_route
   if (!encode_tmap_2d_bf16(&mX, x, (uint64_t)p.hu, (uint64_t)p.Tu, kRtBK, kRtBM) ||
       !encode_tmap_2d_bf16(&mW, wsrc, (uint64_t)Ew, (uint64_t)p.hu, 64, kRtBK))
     return cudaErrorInvalidValue;
-  RouteTcParams g;
+  RouteTcParams g = {};
   g.Tu = p.Tu;
   g.E = p.E;
   g.Np = r.Np;
@@ -396,27 +643,41 @@ cudaError_t launch_route_tc(const Problem& p, const void* x, const void* w_route
   g.status = status;
   const bool warp_sel = p.E > 64;
   const int epl = !warp_sel ? 0 : (p.E <= 128 ? 4 : 8);
+  const unsigned grid = (unsigned)(r.m_tiles * r.S);
+  const int kb = p.K <= 2 ? 2 : (p.K <= 4 ? 4 : 8);
+  if (!p.sigmoid && p.n_groups == 1 && p.E <= 64) {
+    // softmax without a group limit, E <= 64: units routed in registers
+    const RtFast F = rt_fast(r.S, p.E);
+    int st = (int)((kRtFastBudget - F.total) / g.stage_bytes);
+    g.stages = st < 2 ? 2 : (st > kRtMaxStages ? kRtMaxStages : st);
+    g.epi_off = (uint32_t)((size_t)g.stages * g.stage_bytes);
+    const size_t smem = (size_t)g.epi_off + F.total + 1024;
+    if (smem > (size_t)kRtFastBudget + 1024) return cudaErrorInvalidConfiguration;
+    if (p.E <= 8) return launch_rt_fast<8>(mX, mW, g, p.K, grid, smem, s, pdl);
+    if (p.E <= 16) return launch_rt_fast<16>(mX, mW, g, p.K, grid, smem, s, pdl);
+    if (p.E <= 32) return launch_rt_fast<32>(mX, mW, g, p.K, grid, smem, s, pdl);
+    return launch_rt_fast<64>(mX, mW, g, p.K, grid, smem, s, pdl);
+  }
+  g.epi_off = 0;
   const RtEpi L = rt_epi(r.S, p.E, epl);
   size_t smem = (size_t)g.stages * g.stage_bytes;
   if (L.total > smem) smem = L.total;
   smem += 1024;
   if (smem > (size_t)kRtStageBudget + 1024) return cudaErrorInvalidConfiguration;
-  const unsigned grid = (unsigned)(r.m_tiles * r.S);
-  const int kb = p.K <= 2 ? 2 : (p.K <= 4 ? 4 : 8);
   if (warp_sel) {
-    if (epl == 4) return p.sigmoid ? launch_rt<4, 8, true>(mX, mW, g, grid, smem, s, pdl)
-                                   : launch_rt<4, 8, false>(mX, mW, g, grid, smem, s, pdl);
-    return p.sigmoid ? launch_rt<8, 8, true>(mX, mW, g, grid, smem, s, pdl)
-                     : launch_rt<8, 8, false>(mX, mW, g, grid, smem, s, pdl);
+    if (epl == 4) return p.sigmoid ? launch_rt<4, 8, true, 0>(mX, mW, g, grid, smem, s, pdl)
+                                   : launch_rt<4, 8, false, 0>(mX, mW, g, grid, smem, s, pdl);
+    return p.sigmoid ? launch_rt<8, 8, true, 0>(mX, mW, g, grid, smem, s, pdl)
+                     : launch_rt<8, 8, false, 0>(mX, mW, g, grid, smem, s, pdl);
   }
   if (p.sigmoid) {
-    if (kb == 2) return launch_rt<0, 2, true>(mX, mW, g, grid, smem, s, pdl);
-    if (kb == 4) return launch_rt<0, 4, true>(mX, mW, g, grid, smem, s, pdl);
-    return launch_rt<0, 8, true>(mX, mW, g, grid, smem, s, pdl);
+    if (kb == 2) return launch_rt<0, 2, true, 0>(mX, mW, g, grid, smem, s, pdl);
+    if (kb == 4) return launch_rt<0, 4, true, 0>(mX, mW, g, grid, smem, s, pdl);
+    return launch_rt<0, 8, true, 0>(mX, mW, g, grid, smem, s, pdl);
   }
-  if (kb == 2) return launch_rt<0, 2, false>(mX, mW, g, grid, smem, s, pdl);
-  if (kb == 4) return launch_rt<0, 4, false>(mX, mW, g, grid, smem, s, pdl);
-  return launch_rt<0, 8, false>(mX, mW, g, grid, smem, s, pdl);
+  if (kb == 2) return launch_rt<0, 2, false, 0>(mX, mW, g, grid, smem, s, pdl);
+  if (kb == 4) return launch_rt<0, 4, false, 0>(mX, mW, g, grid, smem, s, pdl);
+  return launch_rt<0, 8, false, 0>(mX, mW, g, grid, smem, s, pdl);
 }
 
 }  // namespace moe

@@ -5,8 +5,9 @@
 //    §4: L_aux = α·E·Σ f_i·P_i; §5: a unit's experts restricted to a few groups]
 //
 // Selection keys: softmax → the fp32 logit itself (TopK acts on x·W_g); sigmoid → σ(l) + b formed
-// in fp64. Ties go to the lower expert index (and lower group index). Gates: softmax over the K
-// picked logits, or σ_i/Σσ over the picks (unbiased).
+// in fp64 (decided in fp32 first where the fp32 margins prove the same outcome). Ties go to the
+// lower expert index (and lower group index). Gates, in fp32: softmax over the K picked logits, or
+// σ_i/Σσ over the picks (unbiased).
 //
 // Used by the fused router kernel (route_tc.cu: logits reduced from the tensor-core partials) and by
 // the kernel that routes given logits (route.cu). Two shapes, both block-level (every thread of the
@@ -47,6 +48,17 @@ __device__ __forceinline__ uint32_t ord32(float f) {
   f = f + 0.0f;
   const uint32_t u = __float_as_uint(f);
   return (u >> 31) ? ~u : (u | 0x80000000u);
+}
+
+// Warp argmax of 32-bit ordered keys over the lanes with `has` set: one reduction and one ballot.
+// On equal keys the lowest such lane wins, so candidates must sit in lanes in index order. Returns
+// the winning lane's idx (0x7fffffff if no lane has a candidate) and, in best, its key.
+__device__ __forceinline__ int warp_argmax_redux(uint32_t key, bool has, int idx, uint32_t& best) {
+  const uint32_t m = __reduce_max_sync(0xffffffffu, has ? key : 0u);
+  const uint32_t w = __ballot_sync(0xffffffffu, has && key == m);
+  best = m;
+  if (!w) return 0x7fffffff;
+  return __shfl_sync(0xffffffffu, idx, __ffs(w) - 1);
 }
 
 __device__ __forceinline__ float unord32(uint32_t u) {
@@ -106,8 +118,8 @@ __device__ void select_rows_thread(const SelectCtx& c, float* lg, int ld, int R,
       chosen |= 1u << bg;
     }
     eligible = 0;
-    for (int e = 0; e < E; ++e)
-      if ((chosen >> (e / gs)) & 1u) eligible |= 1ull << e;
+    for (int g = 0, e0 = 0; g < c.n_groups; ++g, e0 += gs)
+      if ((chosen >> g) & 1u) eligible |= (gs >= 64 ? ~0ull : ((1ull << gs) - 1ull)) << e0;
   }
 
   // Top-K: experts in index order into bk[0..K) kept sorted by key, descending. A new key goes
@@ -137,12 +149,12 @@ __device__ void select_rows_thread(const SelectCtx& c, float* lg, int ld, int R,
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) lv[j] = (j < K && be[j] >= 0) ? row[be[j]] : 0.f;
   if (SIGMOID) {
-    double sg[KMAX], z = 0.0;
+    float sg[KMAX], z = 0.f;
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) { sg[j] = (j < K) ? sigmoid64(lv[j]) : 0.0; z += sg[j]; }
+    for (int j = 0; j < KMAX; ++j) { sg[j] = (j < K) ? 1.0f / (1.0f + expf(-lv[j])) : 0.f; z += sg[j]; }
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
-      if (j < K) { c.idx[u * K + j] = be[j]; c.gate[u * K + j] = (float)(sg[j] / z); }
+      if (j < K) { c.idx[u * K + j] = be[j]; c.gate[u * K + j] = sg[j] / z; }
   } else {
     float ev[KMAX], z = 0.f;
 #pragma unroll
@@ -179,6 +191,10 @@ __device__ void select_rows_warp(const SelectCtx& c, float* lg, int ld, int R, i
   const int E = c.E, K = c.K;
   const int gs = E / c.n_groups;
   double* kdbl_w = reinterpret_cast<double*>(gscratch) + (size_t)warp * EP;
+  // group of each of this lane's experts (integer division once, not in every argmax round)
+  int grp[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) grp[j] = (lane * EPL + j) / gs;
   for (int r = warp; r < R; r += nw) {
     const int64_t u = u0 + r;
     float* row = lg + r * ld;
@@ -197,6 +213,7 @@ __device__ void select_rows_warp(const SelectCtx& c, float* lg, int ld, int R, i
     int sel_e = -1;
     bool screened = false;
     uint32_t chosen = 0xffffffffu;
+    float sgm[EPL];  // σ(l) in fp32 (sigmoid scoring): the screen's keys and the unit's P_i
     if (SIGMOID) {
       constexpr float kDelta = 1e-6f;
       float k32[EPL];
@@ -204,34 +221,59 @@ __device__ void select_rows_warp(const SelectCtx& c, float* lg, int ld, int R, i
 #pragma unroll
       for (int j = 0; j < EPL; ++j) {
         const int e = lane * EPL + j;
-        k32[j] = valid[j] ? (1.0f / (1.0f + expf(-lv[j]))) + (c.select_bias ? c.select_bias[e] : 0.0f) : -INFINITY;
+        sgm[j] = valid[j] ? 1.0f / (1.0f + expf(-lv[j])) : 0.0f;
+        k32[j] = valid[j] ? sgm[j] + (c.select_bias ? c.select_bias[e] : 0.0f) : -INFINITY;
         o32[j] = ord32(k32[j]);
       }
       bool safe = true;
       if (c.n_groups > 1) {
-        float* gk = reinterpret_cast<float*>(kdbl_w);
-#pragma unroll
-        for (int j = 0; j < EPL; ++j) gk[lane * EPL + j] = k32[j];
-        __syncwarp();
+        // group scores: the sum of each group's two largest keys
         uint32_t gord = 0;
+        bool gcand = false;
         int gidx = 0x7fffffff;
-        if (lane < c.n_groups) {
+        const int lpg = gs / EPL;  // lanes per group when groups are whole lanes
+        if (gs % EPL == 0 && (lpg & (lpg - 1)) == 0) {
+          // a group is lpg adjacent lanes: local top-2, then a butterfly over the group's lanes
           float t1 = -INFINITY, t2 = -INFINITY;
-          for (int i = 0; i < gs; ++i) {
-            const float v = gk[lane * gs + i];
+#pragma unroll
+          for (int j = 0; j < EPL; ++j) {
+            const float v = k32[j];
             if (v > t1) { t2 = t1; t1 = v; }
             else if (v > t2) t2 = v;
           }
+          for (int o = 1; o < lpg; o <<= 1) {
+            const float b1 = __shfl_xor_sync(0xffffffffu, t1, o), b2 = __shfl_xor_sync(0xffffffffu, t2, o);
+            const float n2 = fmaxf(fminf(t1, b1), fmaxf(t2, b2));
+            t1 = fmaxf(t1, b1);
+            t2 = n2;
+          }
+          gcand = (lane % lpg) == 0 && lane / lpg < c.n_groups;
           gord = ord32(gs > 1 ? t1 + t2 : t1);
-          gidx = lane;
+          gidx = lane / lpg;
+        } else {
+          float* gk = reinterpret_cast<float*>(kdbl_w);
+#pragma unroll
+          for (int j = 0; j < EPL; ++j) gk[lane * EPL + j] = k32[j];
+          __syncwarp();
+          if (lane < c.n_groups) {
+            float t1 = -INFINITY, t2 = -INFINITY;
+            for (int i = 0; i < gs; ++i) {
+              const float v = gk[lane * gs + i];
+              if (v > t1) { t2 = t1; t1 = v; }
+              else if (v > t2) t2 = v;
+            }
+            gord = ord32(gs > 1 ? t1 + t2 : t1);
+            gidx = lane;
+            gcand = true;
+          }
+          __syncwarp();
         }
-        __syncwarp();
         chosen = 0;
         float last_sc = 0.f;
         for (int q = 0; q <= c.topk_groups && q < c.n_groups; ++q) {
-          const bool cand = gidx != 0x7fffffff && !((chosen >> lane) & 1u);
+          const bool cand = gcand && !((chosen >> gidx) & 1u);
           uint32_t bk;
-          const int bg = warp_argmax32(cand ? gord : 0u, cand ? gidx : 0x7fffffff, bk);
+          const int bg = warp_argmax_redux(gord, cand, gidx, bk);
           const float sc = unord32(bk);
           if (q < c.topk_groups) {
             chosen |= 1u << bg;
@@ -241,31 +283,35 @@ __device__ void select_rows_warp(const SelectCtx& c, float* lg, int ld, int R, i
           }
         }
       }
-      bool taken[EPL];
+      // Top-(K+1) over the eligible keys: each lane sorts its candidates once on (key desc, index
+      // asc) — key in the high word, inverted index in the low word, 0 for none — then every round
+      // compares the lanes' heads and the winning lane drops its head.
+      uint64_t cand[EPL];
 #pragma unroll
-      for (int j = 0; j < EPL; ++j) taken[j] = false;
+      for (int j = 0; j < EPL; ++j)
+        cand[j] = (valid[j] && ((chosen >> grp[j]) & 1u))
+                      ? ((uint64_t)o32[j] << 32) | (uint64_t)(~(uint32_t)(lane * EPL + j))
+                      : 0ull;
+#pragma unroll
+      for (int ps = 0; ps < EPL; ++ps)
+#pragma unroll
+        for (int i = ps & 1; i + 1 < EPL; i += 2)
+          if (cand[i] < cand[i + 1]) { const uint64_t t = cand[i]; cand[i] = cand[i + 1]; cand[i + 1] = t; }
       float prev = 0.f;
       for (int q = 0; q <= K; ++q) {
-        uint32_t bk = 0;
-        int be = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < EPL; ++j) {
-          const int e = lane * EPL + j;
-          const bool elig = valid[j] && !taken[j] && ((chosen >> (e / gs)) & 1u);
-          if (elig && (be == 0x7fffffff || o32[j] > bk)) { bk = o32[j]; be = e; }
-        }
+        const bool has = cand[0] != 0ull;
         uint32_t wk;
-        be = warp_argmax32(bk, be, wk);
+        const int be = warp_argmax_redux((uint32_t)(cand[0] >> 32), has, (int)(~(uint32_t)cand[0]), wk);
         if (be == 0x7fffffff) break;  // fewer than K+1 eligible experts: no further margin
         const float kv = unord32(wk);
         if (q > 0 && !(prev - kv > 2.0f * kDelta)) safe = false;
         prev = kv;
-        if (q < K) {
+        if (has && (int)(~(uint32_t)cand[0]) == be) {
 #pragma unroll
-          for (int j = 0; j < EPL; ++j)
-            if (be == lane * EPL + j) taken[j] = true;
-          if (lane == q) sel_e = be;
+          for (int j = 0; j + 1 < EPL; ++j) cand[j] = cand[j + 1];
+          cand[EPL - 1] = 0ull;
         }
+        if (q < K && lane == q) sel_e = be;
       }
       screened = safe;
     }
@@ -323,7 +369,7 @@ __device__ void select_rows_warp(const SelectCtx& c, float* lg, int ld, int R, i
 #pragma unroll
         for (int j = 0; j < EPL; ++j) {
           const int e = lane * EPL + j;
-          const bool elig = valid[j] && !taken[j] && ((chosen >> (e / gs)) & 1u);
+          const bool elig = valid[j] && !taken[j] && ((chosen >> grp[j]) & 1u);
           if (elig && (be == 0x7fffffff || ko[j] > bk)) { bk = ko[j]; be = e; }
         }
 #pragma unroll
@@ -343,11 +389,11 @@ __device__ void select_rows_warp(const SelectCtx& c, float* lg, int ld, int R, i
     const float l_top = __shfl_sync(0xffffffffu, l_sel, 0);
     float g;
     if (SIGMOID) {
-      const double s = (lane < K) ? sigmoid64(l_sel) : 0.0;
-      double z = s;
+      const float s = (lane < K) ? 1.0f / (1.0f + expf(-l_sel)) : 0.0f;
+      float z = s;
 #pragma unroll
       for (int d = 16; d; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
-      g = (float)(s / z);
+      g = s / z;
     } else {
       const float ev = (lane < K) ? expf(l_sel - l_top) : 0.f;
       float z = ev;
@@ -370,7 +416,7 @@ __device__ void select_rows_warp(const SelectCtx& c, float* lg, int ld, int R, i
     }
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
-      pv[j] = !valid[j] ? 0.f : (SIGMOID ? 1.0f / (1.0f + expf(-lv[j])) : expf(lv[j] - m));
+      pv[j] = !valid[j] ? 0.f : (SIGMOID ? sgm[j] : expf(lv[j] - m));
       z += pv[j];
     }
 #pragma unroll
@@ -380,6 +426,98 @@ __device__ void select_rows_warp(const SelectCtx& c, float* lg, int ld, int R, i
     for (int j = 0; j < EPL; ++j)
       if (valid[j]) row[lane * EPL + j] = pv[j] / z;
     __syncwarp();
+  }
+}
+
+// ============================================================================ thread per unit, registers
+// Softmax scoring without a group limit, E <= EMAX <= 64: the unit's fp32 logits (bias included) are
+// in registers l[0..E). Top-K by K rounds of a pairwise tree argmax over (key desc, index asc) — at
+// every level the left operand holds the lower indices, so an equal key keeps the lower index —
+// with the experts already taken masked out. Gates: softmax over the picked logits (the root of each
+// round carries its logit). p[e]: the unit's probabilities over all E experts (zero past E).
+template <int EMAX, int KMAX>
+__device__ __forceinline__ void route_unit_regs(const float (&l)[EMAX], int E, int K, int (&pk)[KMAX],
+                                                float (&gv)[KMAX], float (&p)[EMAX]) {
+  uint64_t taken = 0;
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    pk[k] = -1;
+    gv[k] = 0.f;
+    if (k >= K) continue;
+    float bv[EMAX];
+    int bi[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+      const bool ok = e < E && !((taken >> e) & 1ull);
+      bv[e] = ok ? l[e] : -INFINITY;
+      bi[e] = ok ? e : 0x7fffffff;
+    }
+#pragma unroll
+    for (int w = 1; w < EMAX; w <<= 1)
+#pragma unroll
+      for (int e = 0; e < EMAX; e += 2 * w) {
+        // take the right operand only if it is valid and strictly better (or the left is invalid)
+        const bool right = bi[e + w] != 0x7fffffff && (bi[e] == 0x7fffffff || bv[e + w] > bv[e]);
+        if (right) { bv[e] = bv[e + w]; bi[e] = bi[e + w]; }
+      }
+    pk[k] = bi[0];
+    gv[k] = bv[0];
+    taken |= 1ull << bi[0];
+  }
+  // gates: softmax over the picked logits (pick 0 holds the largest)
+  const float top = gv[0];
+  float z = 0.f;
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k)
+    if (k < K) { gv[k] = expf(gv[k] - top); z += gv[k]; }
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k)
+    if (k < K) gv[k] = gv[k] / z;
+  // probabilities over all experts
+  float m = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < EMAX; ++e)
+    if (e < E) m = fmaxf(m, l[e]);
+  float zs = 0.f;
+#pragma unroll
+  for (int e = 0; e < EMAX; ++e) {
+    p[e] = e < E ? __expf(l[e] - m) : 0.f;
+    zs += p[e];
+  }
+  const float iz = 1.f / zs;
+#pragma unroll
+  for (int e = 0; e < EMAX; ++e) p[e] *= iz;
+}
+
+// Sum of v[e] over the 32 lanes of the warp for every e < EMAX, by a butterfly reduce-scatter (fp32
+// addition is commutative, so each result is one fixed function of the inputs). On return lane L
+// holds, in v[0..max(1, EMAX/32)), the sums of experts [L·EMAX/32, (L+1)·EMAX/32) when EMAX >= 32,
+// or, when EMAX < 32, the sum of expert L / (32/EMAX) (every lane of a group of 32/EMAX lanes holds
+// it).
+template <int LEN>
+__device__ __forceinline__ void rs_step(float* v, int lane, int o) {
+  const bool upper = (lane & o) != 0;
+#pragma unroll
+  for (int j = 0; j < LEN / 2; ++j) {
+    const float send = upper ? v[j] : v[j + LEN / 2];
+    const float keep = upper ? v[j + LEN / 2] : v[j];
+    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+  }
+}
+
+template <int EMAX>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[EMAX], int lane) {
+  static_assert(EMAX == 8 || EMAX == 16 || EMAX == 32 || EMAX == 64, "EMAX");
+  // step i halves the live length (EMAX >> i) across lane offset 16 >> i
+  rs_step<EMAX>(v, lane, 16);
+  rs_step<EMAX / 2>(v, lane, 8);
+  rs_step<EMAX / 4>(v, lane, 4);
+  if constexpr (EMAX >= 16) rs_step<EMAX / 8>(v, lane, 2);
+  if constexpr (EMAX >= 32) rs_step<EMAX / 16>(v, lane, 1);
+  // below 32 experts, the lanes that hold the same expert (offsets under 32/EMAX) add their values
+  if constexpr (EMAX < 32) {
+#pragma unroll
+    for (int o = (32 / EMAX) >> 1; o; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
   }
 }
 
@@ -410,11 +548,12 @@ __device__ __forceinline__ void column_sums(const float* lg, int ld, int R, int 
 // Places of the picks within the tile: rank[r][k] = number of (r', k') with r' < r and the same
 // expert (a unit's picks are distinct, so this is the unit-order queue of the expert within the
 // tile); -1 for a pick of -1. hist[e] = picks of expert e in the tile. lanes_of / warp_pre: shared,
-// blockDim/32 · E entries each. Ends with a block barrier.
+// ceil(R/32) · E entries each (R <= blockDim). Ends with a block barrier.
 __device__ __forceinline__ void rank_picks(const int* picks, int R, int K, int E, int* rank, int* hist,
                                            uint32_t* lanes_of, int* warp_pre) {
   constexpr int kstride = kPickStride;
-  const int t = threadIdx.x, nt = blockDim.x, nw = nt >> 5, w = t >> 5, lane = t & 31;
+  // only the warps that hold rows take part: ceil(R/32) of them
+  const int t = threadIdx.x, nt = blockDim.x, nw = (R + 31) >> 5, w = t >> 5, lane = t & 31;
   for (int i = t; i < nw * E; i += nt) lanes_of[i] = 0u;
   __syncthreads();
   if (t < R)
