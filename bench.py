@@ -209,6 +209,66 @@ class ClockSampler:
                 "samples": len(sel), "window": window}
 
 
+class NvmlClockSampler(ClockSampler):
+    """The same record from NVML in a sampling thread every 5 ms (a 40 ms timed region then holds
+    several samples); falls back to nvidia-smi when NVML cannot be opened."""
+    REASON_BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x4: "sw_power_cap"}
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        super().__init__(device_index)
+        self.period = period_s
+        self.samples = []  # (timestamp, sm_mhz, max_mhz, reason bitmask)
+        self._thread = None
+        self._stop = None
+        self._nvml = None
+
+    def start(self):
+        import threading
+        try:
+            import pynvml as nv
+            nv.nvmlInit()
+            h = nv.nvmlDeviceGetHandleByIndex(self.dev)
+            reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            max_mhz = float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM))
+        except Exception:
+            return super().start()
+        self._nvml = nv
+        self._stop = threading.Event()
+
+        def loop():
+            while not self._stop.is_set():
+                try:
+                    self.samples.append((time.time(), float(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)),
+                                         max_mhz, int(reasons(h))))
+                except Exception:
+                    pass
+                self._stop.wait(self.period)
+
+        self._thread = threading.Thread(target=loop, daemon=True)
+        self._thread.start()
+        return self
+
+    def stop(self):
+        if self._thread is None:
+            return super().stop()
+        self._stop.set()
+        self._thread.join(timeout=5)
+        try:
+            self._nvml.nvmlShutdown()
+        except Exception:
+            pass
+
+    def _rows(self):
+        if self._thread is None:
+            return super()._rows()
+        order = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        bit = {v: k for k, v in self.REASON_BITS.items()}
+        return [(ts, mhz, mx, ["Active" if (mask & bit[n]) else "Not Active" for n in order])
+                for ts, mhz, mx, mask in self.samples]
+
+
 # ------------------------------------------------------------------------------------ inputs
 def device_inputs(shape, device):
     from mixture_experts_layer_96_b300 import LayerWeights
@@ -237,52 +297,59 @@ def kept_rows(shape):
 
 
 # ------------------------------------------------------------------------------------ CPU oracle
-class OracleRun:
-    """The oracle on a bounded sample: it routes all units (capacity is global), then computes the
-    experts and the combine for `n_sample` units. Inputs (and the float64 widening of the expert
-    weights the sample needs) are prepared once, untimed, like resident inputs on the GPU."""
+def default_oracle_tokens(shape) -> int:
+    """Tokens per oracle step: the whole batch for small layers, else a sub-batch of about 3e11
+    expert FLOP (about half a second of float64 BLAS on a GPU server's host cores)."""
+    per_token = 6.0 * shape.h_unit * shape.d_ff * shape.K * shape.n_heads
+    return int(max(16, min(shape.T, 3e11 // per_token)))
 
-    def __init__(self, shape, n_sample: int, seed: int = 0):
+
+class OracleSubBatch:
+    """The oracle's whole layer forward on a sub-batch: the workload's first `n_tokens` tokens taken
+    as a batch of their own (routing, capacity and aux loss over those tokens), with the workload's
+    weights. Inputs are widened to float64 before timing, like inputs resident on the GPU; expert
+    weights too, unless the experts the sub-batch routes to exceed `widen_budget_gb`, in which case
+    the oracle widens each expert when it needs it, inside the timed step."""
+
+    def __init__(self, shape, n_tokens: int, seed: int = 0, widen_budget_gb: float = 24.0):
         import oracle.moe_oracle as O
         self.O = O
         self.shape = shape
+        self.n = int(min(n_tokens, shape.T))
         g = Generator(shape, seed)
+        self.g = g
         bf = shape.dtype == "bf16"
-        f64 = (lambda a: bf16_bits_to_f32(a).astype(np.float64)) if bf else (lambda a: np.asarray(a, np.float64))
-        self.x = f64(g.x())
-        self.wg = f64(g.w_router())
+        self.f64 = (lambda a: bf16_bits_to_f32(a).astype(np.float64)) if bf else (lambda a: np.asarray(a, np.float64))
+        self.x = self.f64(g.x()[: self.n])
+        self.wg = self.f64(g.w_router())
         self.kw = dict(E=shape.E, K=shape.K, score=shape.score, n_heads=shape.n_heads, n_groups=shape.n_groups,
                        topk_groups=shape.topk_groups, capacity_factor=shape.capacity_factor,
                        aux_alpha=shape.aux_alpha, logit_bias=g.logit_bias(), select_bias=g.select_bias())
-        rng = np.random.default_rng(1)
-        self.n = n_sample
-        self.sample = np.sort(rng.choice(shape.T_units, size=n_sample, replace=False))
-        r = O.forward(self.x, self.wg, lambda e: None, sample_units=self.sample[:0], **self.kw)
-        need = sorted({int(e) for u in self.sample for e in r.idx[u]})
+        r = O.forward(self.x, self.wg, lambda e: None, sample_units=np.zeros(0, np.int64), **self.kw)
+        need = sorted(int(e) for e in np.unique(r.idx))
+        per_expert = 3.0 * shape.d_ff * shape.h_unit * 8
         self.cache = {}
-        for e in need:
-            w1, w3, w2 = g.expert(e)
-            self.cache[e] = (f64(w1), f64(w3), f64(w2))
+        self.prewidened = len(need) * per_expert <= widen_budget_gb * 1e9
+        if self.prewidened:
+            for e in need:
+                self.cache[e] = tuple(self.f64(w) for w in g.expert(e))
 
-    def step(self):
-        """(seconds of the routing pass, seconds per sampled unit of experts + combine)."""
-        O = self.O
+    def _expert(self, e):
+        if e in self.cache:
+            return self.cache[e]
+        return tuple(self.f64(w) for w in self.g.expert(e))
+
+    def step(self) -> float:
+        """Seconds of one oracle forward over the sub-batch."""
         t0 = time.perf_counter()
-        O.forward(self.x, self.wg, lambda e: self.cache[e], sample_units=self.sample[:0], **self.kw)
-        t_route = time.perf_counter() - t0
-        t0 = time.perf_counter()
-        O.forward(self.x, self.wg, lambda e: self.cache[e], sample_units=self.sample, **self.kw)
-        t_all = time.perf_counter() - t0
-        return t_route, max(t_all - t_route, 1e-9) / self.n
+        self.O.forward(self.x, self.wg, self._expert, **self.kw)
+        return time.perf_counter() - t0
 
-    def full_batch_seconds(self, t_route, per_unit):
-        return t_route + per_unit * self.shape.T_units
-
-    def describe(self, t_route, per_unit):
+    def describe(self) -> str:
         s = self.shape
-        return (f"float64 numpy oracle: routing of all {s.T_units} units ({t_route:.3f} s) plus expert SwiGLU + "
-                f"combine for {self.n} sampled units ({per_unit:.3f} s/unit), scaled to the {s.T}-token batch; "
-                f"expert weights widened to float64 before timing")
+        how = "weights widened before timing" if self.prewidened else "expert weights widened inside the step"
+        return (f"float64 numpy oracle: the whole layer forward on the first {self.n} of the {s.T} tokens as "
+                f"their own batch ({s.T_units // s.T * self.n} routed units), {how}")
 
 
 def blas_threads():
@@ -298,36 +365,36 @@ def blas_threads():
         return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
 
 
-def cpu_baseline_leg(shape, n_sample):
-    run = OracleRun(shape, min(n_sample, shape.T_units))
-    t_route, per_unit = run.step()
-    v = shape.T / run.full_batch_seconds(t_route, per_unit)
-    out = {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-           "sample": run.describe(t_route, per_unit)}
+def cpu_baseline_leg(shape, n_tokens):
+    """The oracle timed like the reference arm: one untimed and two timed sub-batch steps."""
+    run = OracleSubBatch(shape, n_tokens)
+    run.step()
+    t = min(run.step(), run.step())
+    out = {"value": run.n / t, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+           "sample": run.describe() + "; best of 2 steps"}
     if shape.dtype == "f32":  # the small layer: also the oracle on one core
         try:
-            out["single_core_value"] = single_core_oracle(shape.name, n_sample)
+            out["single_core_value"] = single_core_oracle(shape.name, n_tokens)
         except Exception as ex:  # a report extra: never lose the line for it
             out["single_core_value"] = None
             out["single_core_error"] = repr(ex)
     return out
 
 
-def oracle_tokens_per_s(name: str, n_sample: int) -> float:
-    shape = WORKLOADS[name]
-    run = OracleRun(shape, min(n_sample, shape.T_units))
-    t_route, per_unit = run.step()
-    return shape.T / run.full_batch_seconds(t_route, per_unit)
+def oracle_tokens_per_s(name: str, n_tokens: int) -> float:
+    run = OracleSubBatch(WORKLOADS[name], n_tokens)
+    run.step()
+    return run.n / min(run.step(), run.step())
 
 
-def single_core_oracle(name: str, n_sample: int, timeout_s: float = 300.0) -> float:
+def single_core_oracle(name: str, n_tokens: int, timeout_s: float = 300.0) -> float:
     """The oracle's tokens/s with its BLAS held to one thread: a fresh interpreter (the thread
     count is fixed when numpy loads) that sees no GPU."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     for k in ("RANK", "LOCAL_RANK", "WORLD_SIZE"):
         env.pop(k, None)
-    code = f"import bench; print(bench.oracle_tokens_per_s({name!r}, {int(n_sample)}))"
+    code = f"import bench; print(bench.oracle_tokens_per_s({name!r}, {int(n_tokens)}))"
     r = subprocess.run([sys.executable, "-c", code], cwd=os.path.dirname(os.path.abspath(__file__)), env=env,
                        capture_output=True, text=True, timeout=timeout_s, check=True)
     return float(r.stdout.strip().splitlines()[-1])
@@ -335,25 +402,28 @@ def single_core_oracle(name: str, n_sample: int, timeout_s: float = 300.0) -> fl
 
 # ------------------------------------------------------------------------------------ reference arm
 def run_reference(args, shape):
+    """The oracle as the reference arm: W untimed and K timed steps, each the oracle's forward on the
+    same sub-batch; value = its tokens / the mean step time (no scaling to the full batch)."""
     _, rank, _ = dist_env()
     if rank != 0:
         return
-    run = OracleRun(shape, min(args.ref_sample, shape.T_units))
-    times, last = [], None
+    n = args.ref_sample if getattr(args, "ref_sample", None) else default_oracle_tokens(shape)
+    run = OracleSubBatch(shape, n)
+    times = []
     for i in range(args.warmup + args.steps):
-        t_route, per_unit = run.step()
+        t = run.step()
         if i >= args.warmup:
-            times.append(run.full_batch_seconds(t_route, per_unit))
-            last = (t_route, per_unit)
+            times.append(t)
     ms = 1000.0 * statistics.mean(times)
-    v = shape.T / (ms / 1000.0)
+    v = run.n / (ms / 1000.0)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generator, the workload's recipe)",
-            "config": {"workload": shape.describe(), "global_batch": shape.T, "l2": "n/a (CPU)"},
+            "config": {"workload": shape.describe(), "tokens_per_step": run.n, "global_batch": shape.T,
+                       "l2": "n/a (CPU)"},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                             "sample": run.describe(*last)},
+                             "sample": run.describe()},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -383,7 +453,7 @@ def train_leg(args, shape, cfg, x, lw, device, flush, stream):
         moe_forward_train(cfg, x, lw, outs, ws=ws, gu=gu, y=y)
         moe_backward(cfg, x, lw, dy, outs, gu, ws=ws, bws=bws, d_aux=1.0, grads=grads)
 
-    clk = ClockSampler(device.index or 0).start()
+    clk = NvmlClockSampler(device.index or 0).start()
     b0 = time.time()
     n_warm = 0
     while n_warm < max(3, args.warmup) or time.time() - b0 < min(args.min_warmup_s, 1.0):
@@ -426,8 +496,8 @@ def train_leg(args, shape, cfg, x, lw, device, flush, stream):
 
 # ------------------------------------------------------------------------------------ our arm
 def run_ours(args, shape):
-    from mixture_experts_layer_96_b300 import (ForwardOutputs, Workspace, launch_count, moe_combine,
-                                               moe_dispatch, moe_expert_ffn, moe_forward, moe_route)
+    from mixture_experts_layer_96_b300 import ForwardOutputs, Workspace, launch_count, moe_forward, moe_forward_profiled
+    from mixture_experts_layer_96_b300.moe import FORWARD_STAGES
     from mixture_experts_layer_96_b300.moe import make_config
 
     world, rank, local = dist_env()
@@ -462,7 +532,7 @@ def run_ours(args, shape):
             dist.barrier()
         torch.cuda.synchronize(device)
 
-    clk = ClockSampler(local).start()
+    clk = NvmlClockSampler(local).start()
     busy0 = time.time()
     n_warm = 0
     while n_warm < max(3, args.warmup) or time.time() - busy0 < args.min_warmup_s:
@@ -512,34 +582,17 @@ def run_ours(args, shape):
     ms_median = aggregate_max(median(step_ms), world, device)
     ws.check()
 
-    # ---- per-stage events (same kernels through the stage entry points)
-    st = {k: [] for k in ("route", "dispatch", "expert_ffn", "combine")}
-    idx = torch.empty((shape.T_units, shape.K), dtype=torch.int32, device=device)
-    gate = torch.empty((shape.T_units, shape.K), dtype=torch.float32, device=device)
-    counts_t = torch.empty(shape.E, dtype=torch.int32, device=device)
-    offsets_t = torch.empty(shape.E + 1, dtype=torch.int32, device=device)
-    slot_of = torch.empty((shape.T_units, shape.K), dtype=torch.int32, device=device)
-    row_token = torch.empty(shape.T_units * shape.K, dtype=torch.int32, device=device)
-    xp = torch.empty((shape.T_units * shape.K, shape.h_unit), dtype=x.dtype, device=device)
-    yp = torch.empty_like(xp)
+    # ---- per-stage events: the same forward with an event at each stage boundary (moe_forward_profiled;
+    # programmatic dependent launch is off between stages there, so the stages' sum exceeds a step)
+    st = {k: [] for k in FORWARD_STAGES}
+    prof = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
     for i in range(args.steps):
         if flush is not None:
             flush.fill_(i & 0xFF)
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-        e[0].record(stream)
-        moe_route(cfg, x, lw.w_router, lw.logit_bias, lw.select_bias, ws=ws, topk_idx=idx, topk_gate=gate,
-                  aux_out=outs.aux)
-        e[1].record(stream)
-        moe_dispatch(cfg, x, idx, ws=ws, counts=counts_t, offsets=offsets_t, slot_of=slot_of,
-                     row_token=row_token, x_packed=xp)
-        e[2].record(stream)
-        moe_expert_ffn(cfg, xp, offsets_t, lw.w_gate, lw.w_up, lw.w_down, ws=ws, y_packed=yp)
-        e[3].record(stream)
-        moe_combine(cfg, yp, slot_of, gate, ws=ws, y=y)
-        e[4].record(stream)
+        moe_forward_profiled(cfg, x, lw, prof, ws=ws, y=y, outputs=outs)
         torch.cuda.synchronize(device)
-        for j, k in enumerate(st):
-            st[k].append(e[j].elapsed_time(e[j + 1]))
+        for j, k in enumerate(FORWARD_STAGES):
+            st[k].append(prof[j].elapsed_time(prof[j + 1]))
     ws.check()
     busy1 = time.time()
     clk.stop()
@@ -600,24 +653,37 @@ def run_ours(args, shape):
             dist.destroy_process_group()
         return
 
-    # ---- roofline of the dominant kernel group (the expert grouped GEMMs)
+    # ---- roofline of the dominant kernel group (the expert grouped GEMMs). Its time inside a timed
+    # forward is the step time times the GEMMs' share of the profiled forward's stages (the stages
+    # run without overlap there), so achieved never exceeds what the timed step allows.
     pk = peaks()
     flops = 6.0 * shape.h_unit * shape.d_ff * kept
-    achieved_tf = flops / (stage_ms["expert_ffn"] * 1e-3) / 1e12
+    stage_sum = sum(stage_ms.values())
+    gemm_share = stage_ms["expert_ffn"] / stage_sum if stage_sum > 0 else 1.0
+    gemm_ms_in_step = ms * gemm_share
+    achieved_tf = flops / (gemm_ms_in_step * 1e-3) / 1e12
+    achieved_profiled_tf = flops / (stage_ms["expert_ffn"] * 1e-3) / 1e12
     # the regime (power-capped or not) is read from the whole busy window: the timed region alone
     # can be shorter than a few samples and catch the clock between power-cap adjustments
     peak_tf, peak_kind = choose_peak(pk, busy_clocks)
     elt = 2 if shape.dtype == "bf16" else 4
-    d_bytes = shape.T_units * shape.h_unit * elt + kept * shape.h_unit * elt + kept * 4 * 2
+    # dispatch: x read, x_packed written, per pick its index and place read and slot written, per
+    # packed row its source unit written
+    d_bytes = shape.T_units * shape.h_unit * elt + kept * shape.h_unit * elt + shape.T_units * shape.K * 12 + \
+        shape.T_units * shape.K * 4
     c_bytes = kept * shape.h_unit * elt + shape.T_units * shape.h_unit * elt + shape.T_units * shape.K * 8
     hbm = float(pk["hbm_gbs"])
-    stages = {
-        "route_ms": stage_ms["route"], "dispatch_ms": stage_ms["dispatch"],
-        "expert_ffn_ms": stage_ms["expert_ffn"], "combine_ms": stage_ms["combine"],
-        "expert_ffn_tflops": achieved_tf,
-        "dispatch_gbs": d_bytes / (stage_ms["dispatch"] * 1e-3) / 1e9,
+    disp_ms = stage_ms["scan"] + stage_ms["pack"]
+    stages = {f"{k}_ms": v for k, v in stage_ms.items()}
+    stages.update({
+        "dispatch_ms": disp_ms, "expert_ffn_tflops_profiled": achieved_profiled_tf,
+        "expert_ffn_share_of_step": gemm_share,
+        "pack_gbs": d_bytes / (stage_ms["pack"] * 1e-3) / 1e9,
+        "dispatch_gbs": d_bytes / (disp_ms * 1e-3) / 1e9,
         "combine_gbs": c_bytes / (stage_ms["combine"] * 1e-3) / 1e9,
-    }
+        "how": "moe_forward_profiled: the forward's own kernels with a CUDA event at each stage boundary",
+    })
+    stages["pack_frac_hbm"] = stages["pack_gbs"] / hbm
     stages["dispatch_frac_hbm"] = stages["dispatch_gbs"] / hbm
     stages["combine_frac_hbm"] = stages["combine_gbs"] / hbm
     value = world * shape.T / (ms * 1e-3)
@@ -633,6 +699,9 @@ def run_ours(args, shape):
                    "cuda_graph": bool(args.graph), "kernels_per_forward": per_forward, "max_over_mean_load": max(counts) / (sum(counts) / len(counts))},
         "roofline": {"bound": "tensor", "kernel": "expert grouped GEMMs (gate/up+SwiGLU and down, 2 launches per forward)",
                      "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved_tf / peak_tf,
+                     "how": "6·h'·d_ff·kept FLOP per forward ÷ (ms_per_step × the GEMMs' share of the profiled "
+                            "forward's stage times)",
+                     "gemm_ms_in_step": gemm_ms_in_step, "achieved_profiled": achieved_profiled_tf,
                      "peak_kind": peak_kind,
                      "frac_of_burst": achieved_tf / float(pk["bf16_tflops"]),
                      "frac_of_sustained": achieved_tf / float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
@@ -653,13 +722,15 @@ def run_ours(args, shape):
     line["roofline"]["frac_of_spec"] = achieved_tf / SPEC_BF16_TFLOPS
     try:  # report extras: on any error the line keeps everything above and says why
         e_active = sum(1 for c in counts if c > 0)
-        lr = layer_roofline(shape, kept, e_active, stage_ms, ms, hbm, peak_tf)
+        lr_stage = {"route": stage_ms["route"], "dispatch": disp_ms, "expert_ffn": stage_ms["expert_ffn"],
+                    "combine": stage_ms["combine"]}
+        lr = layer_roofline(shape, kept, e_active, lr_stage, ms, hbm, peak_tf)
         line["layer_roofline"] = lr
         if lr["gemm_bound"] == "hbm":
             # the GEMMs stream more weight bytes than their FLOP take at the tensor peak: the HBM
             # roofline grades them; the tensor view stays in the line
             gb = gemm_bytes(shape, kept, e_active)
-            ach = gb / (stage_ms["expert_ffn"] * 1e-3) / 1e9
+            ach = gb / (gemm_ms_in_step * 1e-3) / 1e9
             tensor_view = dict(line["roofline"])
             line["roofline"] = {"bound": "hbm", "kernel": tensor_view["kernel"], "achieved": ach, "peak": hbm,
                                 "unit": "GB/s", "frac": ach / hbm, "algorithmic_bytes": gb,
@@ -672,7 +743,7 @@ def run_ours(args, shape):
         train["backward_frac_of_sustained_whole"] = train["backward_tflops_whole"] / bw_peak
         line["train"] = train
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_leg(shape, args.cpu_sample)
+        line["cpu_baseline"] = cpu_baseline_leg(shape, args.cpu_sample or default_oracle_tokens(shape))
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -686,8 +757,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral_bf16", choices=sorted(WORKLOADS))
-    ap.add_argument("--cpu-sample", type=int, default=4096, help="units the CPU-baseline oracle computes (capped at the batch)")
-    ap.add_argument("--ref-sample", type=int, default=32, help="units per reference-arm step (about 0.5 s each)")
+    ap.add_argument("--cpu-sample", type=int, default=None,
+                    help="tokens per CPU-baseline oracle step (default: the whole batch, or ~1e11 expert FLOP)")
+    ap.add_argument("--ref-sample", type=int, default=None,
+                    help="tokens per reference-arm step (default as --cpu-sample)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", dest="graph", action="store_true", default=True,
                     help="replay the forward from a CUDA graph in the timed loop (default)")

@@ -166,6 +166,17 @@ MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const void* y_packed, 
 MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
                          const moe_outputs_t* out, void* ws, moe_stream_t stream);
 
+/* moe_forward with a CUDA event recorded on `stream` at each boundary between its stages, for
+ * timing them (instrumentation; the pages have no counterpart). events: 6 caller-created cudaEvent_t
+ * (as void*), recorded before the routing, after the routing, after the scan (counts, offsets, aux
+ * loss), after the pack, after the expert GEMMs and after the combine. The kernels are the same as
+ * moe_forward's, but neighbouring stages no longer overlap their launch (programmatic dependent
+ * launch is off), so the sum of the stage times can exceed a moe_forward call's time.
+ * MOE_ERR_INVALID_ARG if events or one of them is NULL. */
+MOE_API moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
+                                          const moe_outputs_t* out, void* ws, void* const* events,
+                                          moe_stream_t stream);
+
 /* ---- training: forward that keeps what the backward needs, and the backward ----------------
  * The pages train this layer ([HAI] §"HAI-LLM 上的使用"; [Lesson 10 §4] adds L_aux to the training
  * loss) but give no backward formulas. The backward here is the gradient of

@@ -270,12 +270,12 @@ static cudaError_t route_stage(const Problem& p, const void* x, const void* w_ro
 
 // The per-expert scan over the routing tiles (counts, offsets, tile bases) and the aux loss.
 static cudaError_t scan_stage(const Problem& p, void* ws, int32_t* counts_out, int32_t* offsets_out, float* aux_out,
-                              cudaStream_t s) {
+                              cudaStream_t s, bool pdl = true) {
   const WsLayout L = ws_layout(p);
   return launch_scan(p, p.ntiles, ws_ptr<int32_t>(ws, L.chunk_hist), aux_out ? ws_ptr<float>(ws, L.psum) : nullptr,
                      ws_ptr<int32_t>(ws, L.chunk_base), ws_ptr<int32_t>(ws, L.counts), ws_ptr<int32_t>(ws, L.offsets),
                      counts_out, offsets_out, ws_ptr<float>(ws, L.aux_terms),
-                     ws_ptr<unsigned int>(ws, L.status + 8), aux_out, s, true);
+                     ws_ptr<unsigned int>(ws, L.status + 8), aux_out, s, pdl);
 }
 
 }  // namespace moe
@@ -367,8 +367,14 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* y_packed, const in
                                     ws_ptr<uint32_t>(ws, L.status), (cudaStream_t)stream));
 }
 
+// events: null, or kForwardEvents cudaEvent_t recorded on the stream before the routing, after it,
+// after the scan, after the pack, after the expert GEMMs and after the combine (then the kernels of
+// neighbouring stages are not overlapped by programmatic dependent launch).
+static constexpr int kForwardEvents = 6;
+
 static moe_status_t forward_impl(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
-                                 const moe_outputs_t* out, void* ws, moe_stream_t stream, void* gu) {
+                                 const moe_outputs_t* out, void* ws, moe_stream_t stream, void* gu,
+                                 void* const* events = nullptr) {
   Problem p;
   const moe_status_t st = make_problem(cfg, &p);
   if (st != MOE_OK) return st;
@@ -393,28 +399,43 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const void* x, const m
   void* y_packed = ws_ptr<void>(ws, L.y_packed);
   uint32_t* status = ws_ptr<uint32_t>(ws, L.status);
 
+  auto mark = [&](int i) -> bool {
+    return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
+  };
+  const bool pdl = events == nullptr;
+  if (!mark(0)) return MOE_ERR_CUDA;
   // routing (each pick's place within its tile goes into slot_of, which the pack turns into slots)
   cudaError_t e = route_stage(p, x, w->w_router, nullptr, w->logit_bias, w->select_bias, idx, gate, o.logits, slot_of,
                               ws, s);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (e != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
   // counts, offsets (into the workspace; the caller's copies are optional) and the aux loss
-  e = scan_stage(p, ws, o.counts, o.offsets, o.aux, s);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = scan_stage(p, ws, o.counts, o.offsets, o.aux, s, pdl);
+  if (e != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
   if (p.rows > 0) {
     e = launch_pack(p, x, idx, kTileShift, ws_ptr<int32_t>(ws, L.chunk_base), offsets_ws, slot_of, row_token, x_packed,
-                    s, true);
+                    s, pdl);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
+  if (!mark(3)) return MOE_ERR_CUDA;
   e = launch_expert_ffn(p, x_packed, offsets_ws, w->w_gate, w->w_up, w->w_down, hidden, y_packed,
-                        status, s, gu, true);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = launch_combine(p, y_packed, slot_of, gate, y, status, s, true);
-  return cuda_status(e);
+                        status, s, gu, pdl);
+  if (e != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
+  e = launch_combine(p, y_packed, slot_of, gate, y, status, s, pdl);
+  if (e != cudaSuccess || !mark(5)) return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
                          const moe_outputs_t* out, void* ws, moe_stream_t stream) {
   return forward_impl(cfg, x, w, y, out, ws, stream, nullptr);
+}
+
+moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
+                                  const moe_outputs_t* out, void* ws, void* const* events, moe_stream_t stream) {
+  if (!events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < kForwardEvents; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  return forward_impl(cfg, x, w, y, out, ws, stream, nullptr, events);
 }
 
 size_t moe_saved_gu_size(const moe_config_t* cfg) {

@@ -25,7 +25,8 @@ MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_capacity", "moe_route", "moe_route_logits",
            "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_status",
            "moe_status_string", "moe_launch_count", "moe_abi_version", "moe_dispatch_noalloc",
-           "moe_saved_gu_size", "moe_forward_train", "moe_backward_workspace_size", "moe_backward")
+           "moe_saved_gu_size", "moe_forward_train", "moe_backward_workspace_size", "moe_backward",
+           "moe_forward_profiled")
 
 
 class MoEError(RuntimeError):
@@ -94,6 +95,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_expert_ffn": (I32, [cfgp, P, P, P, P, P, P, P, P]),
         "moe_combine": (I32, [cfgp, P, P, P, P, P, P]),
         "moe_forward": (I32, [cfgp, P, ctypes.POINTER(MoEWeights), P, ctypes.POINTER(MoEOutputs), P, P]),
+        "moe_forward_profiled": (I32, [cfgp, P, ctypes.POINTER(MoEWeights), P, ctypes.POINTER(MoEOutputs), P,
+                                       ctypes.POINTER(ctypes.c_void_p), P]),
         "moe_get_status": (I32, [P, P]),
         "moe_status_string": (ctypes.c_char_p, [I32]),
         "moe_launch_count": (ctypes.c_uint64, []),
@@ -408,6 +411,36 @@ def moe_forward(cfg: MoEConfig, x, weights: LayerWeights, *, ws: Workspace, y=No
     _check(_run([x, y, ws.buf, *weights.tensors(), *(outputs.tensors() if outputs is not None else ())], stream,
                 lib.moe_forward, ctypes.byref(cfg), _ptr(x), ctypes.byref(cw), _ptr(y),
                 ctypes.byref(co) if co is not None else None, ws.ptr), "moe_forward")
+    return y
+
+
+FORWARD_STAGES = ("route", "scan", "pack", "expert_ffn", "combine")
+
+
+def moe_forward_profiled(cfg: MoEConfig, x, weights: LayerWeights, events, *, ws: Workspace, y=None,
+                         outputs: Optional[ForwardOutputs] = None, stream=None):
+    """moe_forward with the 6 given torch.cuda.Event (enable_timing=True) recorded at its stage
+    boundaries: event i → i+1 brackets FORWARD_STAGES[i]. Returns y."""
+    lib = load_library()
+    dt = cfg.torch_dtype
+    _req(x, "x", (cfg.T, cfg.h), dt)
+    weights.check(cfg)
+    if len(events) != 6:
+        raise ValueError("moe_forward_profiled takes 6 events")
+    y = y if y is not None else torch.empty((cfg.T, cfg.h), dtype=dt, device=x.device)
+    _req(y, "y", (cfg.T, cfg.h), dt)
+    dev = _one_device(x, y)
+    with torch.cuda.device(dev):
+        st = torch.cuda.current_stream(dev) if stream is None else stream
+        for ev in events:  # torch creates the CUDA event at its first record
+            if not ev.cuda_event:
+                ev.record(st)
+        handles = (ctypes.c_void_p * 6)(*[ev.cuda_event for ev in events])
+    cw = weights.c_struct()
+    co = outputs.c_struct() if outputs is not None else None
+    _check(_run([x, y, ws.buf, *weights.tensors(), *(outputs.tensors() if outputs is not None else ())], stream,
+                lib.moe_forward_profiled, ctypes.byref(cfg), _ptr(x), ctypes.byref(cw), _ptr(y),
+                ctypes.byref(co) if co is not None else None, ws.ptr, handles), "moe_forward_profiled")
     return y
 
 

@@ -135,3 +135,37 @@ def test_cpu_baseline_adds_a_single_core_time_for_the_f32_layer():
     cb = bench.cpu_baseline_leg(bench.WORKLOADS["tiny_f32"], 8)
     assert cb["kind"] == "oracle" and cb["value"] > 0
     assert cb["single_core_value"] is not None and cb["single_core_value"] > 0
+
+
+def test_nvml_sampler_reads_reason_bits():
+    """NVML samples (timestamp, SM MHz, max MHz, clock-event reason bits) summarise like the
+    nvidia-smi record: median clock inside the window and the active slowdown reasons."""
+    c = bench.NvmlClockSampler(0)
+    c._thread = object()  # as if the sampling thread had run
+    t = 1000.0
+    c.samples = [(t, 1900.0, 2032.0, 0x0), (t + 0.01, 1300.0, 2032.0, 0x4), (t + 0.02, 1200.0, 2032.0, 0x4 | 0x40),
+                 (t + 5.0, 500.0, 2032.0, 0x8)]
+    s = c.summary(t - 0.001, t + 0.03, t - 1, t + 10)
+    assert s["samples"] == 3 and s["sm_mhz"] == 1300
+    assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+
+
+def test_reference_arm_times_a_real_sub_batch(monkeypatch, capsys):
+    """No scaling: value × the step time is the number of tokens each step runs."""
+    import json
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+
+    class A:
+        ref_sample, steps, warmup, gpus = 64, 2, 1, 1
+    bench.run_reference(A(), bench.WORKLOADS["tiny_f32"])
+    line = json.loads(capsys.readouterr().out.strip())
+    assert line["config"]["tokens_per_step"] == 64
+    assert line["value"] * line["ms_per_step"] / 1000.0 == pytest.approx(64, rel=1e-9)
+
+
+def test_oracle_sub_batch_sizes():
+    # whole batch for the small layer; a bounded sub-batch for the benchmark layer
+    assert bench.default_oracle_tokens(bench.WORKLOADS["tiny_f32"]) == 256
+    n = bench.default_oracle_tokens(bench.WORKLOADS["mixtral_bf16"])
+    assert 64 <= n < 4096

@@ -175,3 +175,25 @@ def test_forward_parity_full_size_sampled(name):
     inp = Inputs.make(shape)
     y, outs = run_forward(inp)
     check_forward(inp, y, outs, sample=tile_covering_sample(256))
+
+
+def test_profiled_forward_gives_the_same_bits_and_ordered_stage_events():
+    """moe_forward_profiled runs the forward's own kernels with an event at each stage boundary: y
+    and the outputs equal moe_forward's bit for bit, and the events bracket five stages."""
+    from mixture_experts_layer_96_b300 import moe_forward_profiled
+    shape = scaled(WORKLOADS["skewed_bf16"], T=2000, h=256, d_ff=384)
+    inp = Inputs.make(shape)
+    cfg = config_of(shape)
+    x, lw = inp.device()
+    ws = Workspace(cfg)
+    o1, o2 = ForwardOutputs.allocate(cfg, "cuda"), ForwardOutputs.allocate(cfg, "cuda")
+    y1 = moe_forward(cfg, x, lw, ws=ws, outputs=o1)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    y2 = moe_forward_profiled(cfg, x, lw, ev, ws=ws, outputs=o2)
+    torch.cuda.synchronize()
+    ws.check()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    for t1, t2 in zip(o1.tensors(), o2.tensors()):
+        assert torch.equal(t1, t2)
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(5)]
+    assert all(t >= 0 for t in times) and sum(times) > 0
