@@ -35,6 +35,8 @@ Readings where the pages are silent (the same list is kept in the design notes):
   R9 Multi-head: x[T][H·h'] is read as T·H sub-tokens x[t·H+j] = x[t, j·h':(j+1)·h'], each routed
      and computed alone with one shared router and expert pool; y is read back the same way.
   R10 Routing from given fp32 logits: a logit bias is added in fp32 (the decision precision).
+  R16 Hash gate: expert = fmix32(token id) mod E (MurmurHash3's finalizer), gate 1, top-1, no aux
+     loss (no routing probabilities); capacity as for any gate.
 
 Parity pins (tests/test_oracle_pins.py): brute-force Top-K and group limit on tiny inputs, a
 brute-force O(T^2) capacity rank, closed forms (aux = α under uniform routing, softmax-over-picks
@@ -371,6 +373,54 @@ def forward(x: np.ndarray, w_g: np.ndarray, experts: ExpertProvider, *, E: int, 
         for (u, k), o in zip(pairs, out):
             acc[u] += g[u, k] * o
     return Result(l, idx, g, keys, d, aux, C, None, acc)
+
+
+# ---------------------------------------------------------------------------------------------
+# [HAI §"HAI-LLM 上的使用"] hash gate (HashGate: top_k == 1 only). The page names the gate and its
+# top-1 limit and nothing more. Reading R16: a hash gate has no learned router; unit u goes to
+# expert fmix32(token_id_u) mod E with gate 1, where fmix32 is MurmurHash3's 32-bit finalizer (a
+# published integer mix, Austin Appleby, public domain). No router means no routing
+# probabilities, so the aux loss is 0. Capacity and drops are as for any gate.
+
+
+def fmix32(h: int) -> int:
+    """MurmurHash3's finalizer of a 32-bit value: xor-shift 16, multiply by 0x85ebca6b, xor-shift 13,
+    multiply by 0xc2b2ae35, xor-shift 16 (all mod 2^32)."""
+    h &= 0xFFFFFFFF
+    h ^= h >> 16
+    h = (h * 0x85EBCA6B) & 0xFFFFFFFF
+    h ^= h >> 13
+    h = (h * 0xC2B2AE35) & 0xFFFFFFFF
+    h ^= h >> 16
+    return h
+
+
+def hash_route(token_ids: np.ndarray, E: int):
+    """(idx [T'][1] int32, gate [T'][1] float64 of ones) for the hash gate.  [HAI; R16]
+
+    token_ids: [T'] integers; each is taken as its 32-bit two's-complement pattern."""
+    ids = np.asarray(token_ids).reshape(-1)
+    idx = np.array([fmix32(int(t) & 0xFFFFFFFF) % E for t in ids], dtype=np.int32).reshape(-1, 1)
+    return idx, np.ones(idx.shape, dtype=np.float64)
+
+
+def forward_hashed(x: np.ndarray, token_ids: np.ndarray, experts: ExpertProvider, *, E: int,
+                   n_heads: int = 1, capacity_factor: Optional[float] = None) -> Result:
+    """The layer with the hash gate: y_u = FFN_{h(u)}(x_u) for a kept unit, 0 for a dropped one;
+    aux = 0.  [HAI; Lesson 10 §3, §4; R16]"""
+    xu = split_heads(x, n_heads)
+    Tu = xu.shape[0]
+    idx, g = hash_route(token_ids, E)
+    C = capacity(capacity_factor, 1, Tu, E)
+    d = dispatch(idx, E, C)
+    y = np.zeros_like(xu)
+    for e in range(E):
+        r0, r1 = int(d.offsets[e]), int(d.offsets[e + 1])
+        if r1 > r0:
+            units = d.row_token[r0:r1]
+            w1, w3, w2 = experts(e)
+            y[units] = expert_ffn(xu[units], w1, w3, w2)
+    return Result(None, idx, g, None, d, 0.0, C, merge_heads(y, n_heads))
 
 
 # ---------------------------------------------------------------------------------------------

@@ -432,3 +432,51 @@ def test_dispatch_pin_catches_le_capacity(monkeypatch):
     monkeypatch.setattr(O, "dispatch", wrong)
     with pytest.raises(AssertionError):
         check_dispatch_bruteforce(O)
+
+
+# ----------------------------------------------------------------------------- hash gate (R16)
+def test_fmix32_published_vectors():
+    """MurmurHash3_x86_32 of the empty input is the finalizer applied to the seed (no blocks, no tail,
+    length 0), so its reference test vectors for the empty input pin the finalizer: seed 1 gives
+    0x514E28B7 and seed 0xFFFFFFFF gives 0x81F16F39; seed 0 gives 0."""
+    assert O.fmix32(1) == 0x514E28B7
+    assert O.fmix32(0xFFFFFFFF) == 0x81F16F39
+    assert O.fmix32(0) == 0
+
+
+def test_fmix32_is_a_bijection_on_a_sample():
+    rng = np.random.default_rng(7)
+    xs = np.unique(rng.integers(0, 2 ** 32, size=200_000, dtype=np.uint64))
+    hs = {O.fmix32(int(v)) for v in xs}
+    assert len(hs) == len(xs)
+
+
+def test_hash_route_is_top1_gate_one_and_balanced():
+    E = 16
+    ids = np.arange(E * 2000)
+    idx, g = O.hash_route(ids, E)
+    assert idx.shape == (E * 2000, 1) and (g == 1.0).all()
+    assert idx.min() >= 0 and idx.max() < E
+    counts = np.bincount(idx[:, 0], minlength=E)
+    sigma = np.sqrt(2000 * (1 - 1 / E))
+    assert np.all(np.abs(counts - 2000) < 6 * sigma)
+    # negative ids hash their 32-bit pattern
+    assert O.hash_route(np.array([-1]), E)[0][0, 0] == O.fmix32(0xFFFFFFFF) % E
+
+
+def test_forward_hashed_equals_top1_layer_at_the_hashed_picks():
+    """With K = 1 a softmax gate over one pick is 1, so the generic layer at the hashed picks must
+    give the hash layer's y (drops included); E = 1 reduces to the dense SwiGLU."""
+    rng = np.random.default_rng(3)
+    T, h, E, F = 40, 12, 4, 10
+    x = rng.normal(size=(T, h))
+    ws = [(rng.normal(size=(F, h)), rng.normal(size=(F, h)), rng.normal(size=(h, F))) for _ in range(E)]
+    ids = rng.integers(0, 50000, size=T)
+    r = O.forward_hashed(x, ids, lambda e: ws[e], E=E, capacity_factor=1.0)
+    idx, _ = O.hash_route(ids, E)
+    g = O.forward(x, rng.normal(size=(h, E)), lambda e: ws[e], E=E, K=1, capacity_factor=1.0, idx_override=idx)
+    np.testing.assert_allclose(r.y, g.y, rtol=1e-12, atol=1e-12)
+    assert r.aux == 0.0 and (r.dispatch.slot_of == g.dispatch.slot_of).all()
+    dense = O.forward_hashed(x, ids, lambda e: ws[0], E=1)
+    w1, w3, w2 = ws[0]
+    np.testing.assert_allclose(dense.y, O.expert_ffn(x, w1, w3, w2), rtol=1e-12, atol=1e-12)
