@@ -146,6 +146,20 @@ MOE_API moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const 
                           int32_t* counts, int32_t* offsets, int32_t* slot_of, int32_t* row_token,
                           void* x_packed, void* ws, moe_stream_t stream);
 
+/* Dispatch of one shard of a batch split by tokens over several processes (a data-parallel layer
+ * whose capacity and drop order are those of the whole batch).          [Lesson 10 §3 step 1, §4]
+ * The shard holds cfg->T of the batch's T_global tokens; earlier shards hold the batch's earlier
+ * tokens. queue_base [E] (device, int32): picks of each expert on all earlier shards — the exclusive
+ * scan over shards of their pre-drop counts, the one exchange step (an all-gather of E int32 per
+ * shard). The capacity is the whole batch's, C = ceil(CF·K·T'_global/E); a pick of this shard at
+ * place p in its expert's local queue is kept iff queue_base[e] + p < C. Outputs as moe_dispatch,
+ * local to the shard (counts are this shard's pre-drop counts; offsets scan this shard's kept
+ * rows). queue_base = 0 and T_global = T is moe_dispatch. */
+MOE_API moe_status_t moe_dispatch_sharded(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
+                                          const int32_t* queue_base, int64_t T_global, int32_t* counts,
+                                          int32_t* offsets, int32_t* slot_of, int32_t* row_token, void* x_packed,
+                                          void* ws, moe_stream_t stream);
+
 /* Per-expert SwiGLU FFN over the packed rows (grouped GEMMs).           [Lesson 10 §3 step 2]
  *  x_packed [T'·K][h'], offsets [E+1] (device; offsets[0] == 0, non-decreasing,
  *  offsets[E] <= T'·K), w_gate/w_up [E][d_ff][h'], w_down [E][h'][d_ff].
@@ -165,6 +179,24 @@ MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const void* y_packed, 
  * `out` may be NULL or have NULL members; intermediates live in `ws`. */
 MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
                          const moe_outputs_t* out, void* ws, moe_stream_t stream);
+
+/* ---- hash gate ------------------------------------------------------------------------------
+ * HAI-LLM offers a HashGate beside its GShard and Switch gates, top_k == 1 only
+ *   ["HAI-LLM MoE：一键实现大模型的混合专家并行训练", §"HAI-LLM 上的使用"]; the page says no more.
+ * Here a hash gate has no learned router: unit u goes to expert fmix32(token_ids[u]) mod E, with
+ * fmix32 MurmurHash3's 32-bit finalizer (xor-shift 16, ·0x85ebca6b, xor-shift 13, ·0xc2b2ae35,
+ * xor-shift 16) of the id's 32-bit pattern, and gate 1. Capacity and drops are as for any gate; with
+ * no routing probabilities there is no aux loss (0). cfg.K must be 1 (else MOE_ERR_UNSUPPORTED);
+ * score, groups and aux_alpha are not used. token_ids: [T'] int32 device array, one id per unit
+ * (with H heads, one per sub-token). */
+MOE_API moe_status_t moe_route_hash(const moe_config_t* cfg, const int32_t* token_ids, int32_t* topk_idx,
+                                    float* topk_gate, void* ws, moe_stream_t stream);
+
+/* The whole layer with the hash gate: moe_forward with the routing above. w->w_router, logit_bias
+ * and select_bias are not used (may be NULL). out->logits is not written; out->aux gets 0. */
+MOE_API moe_status_t moe_forward_hash(const moe_config_t* cfg, const void* x, const int32_t* token_ids,
+                                      const moe_weights_t* w, void* y, const moe_outputs_t* out, void* ws,
+                                      moe_stream_t stream);
 
 /* moe_forward with a CUDA event recorded on `stream` at each boundary between its stages, for
  * timing them (instrumentation; the pages have no counterpart). events: 6 caller-created cudaEvent_t

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kScanThreads)
 scan_kernel(const int32_t* __restrict__ hist, int64_t nchunks, int E, int64_t C, const float* __restrict__ psum,
             int64_t Tu, int K, float alpha, int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts_ws,
             int32_t* __restrict__ offsets_ws, int32_t* counts_out, int32_t* offsets_out, float* terms,
-            unsigned int* ticket, float* aux_out) {
+            unsigned int* ticket, float* aux_out, const int32_t* __restrict__ qbase, int64_t* __restrict__ cap_out) {
   __shared__ int warp_tot[kScanThreads / 32];
   __shared__ long long warp_p[kScanThreads / 32];
   __shared__ int excl[kMaxExperts + 1];
@@ -124,6 +124,9 @@ scan_kernel(const int32_t* __restrict__ hist, int64_t nchunks, int E, int64_t C,
   if (tid == 0) {
     counts_ws[e] = carry;
     if (counts_out) counts_out[e] = carry;
+    // a shard of a larger batch: this expert's queue already holds qbase[e] picks of earlier ranks,
+    // so the capacity left here is C - qbase[e]
+    if (qbase) cap_out[e] = C == INT64_MAX ? C : C - (int64_t)qbase[e];
     if (psum) {
       long long P = 0;
       for (int w = 0; w < kScanThreads / 32; ++w) P += warp_p[w];
@@ -145,7 +148,9 @@ scan_kernel(const int32_t* __restrict__ hist, int64_t nchunks, int E, int64_t C,
       loc[j] = sum;
       if (ee < E) {
         const int64_t n = cnt[ee];
-        sum += (int)(n < C ? n : C);
+        int64_t cap = (qbase && C != INT64_MAX) ? C - (int64_t)qbase[ee] : C;
+        if (cap < 0) cap = 0;
+        sum += (int)(n < cap ? n : cap);
       }
     }
     int incl = sum;
@@ -186,8 +191,8 @@ scan_kernel(const int32_t* __restrict__ hist, int64_t nchunks, int E, int64_t C,
 // row_token -1.
 __global__ void __launch_bounds__(256)
 pack_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ idx, const int32_t* __restrict__ chunk_base,
-            const int32_t* __restrict__ offsets, int64_t Tu, int K, int E, int64_t C, int chunk_shift,
-            int row_vecs, int64_t rows, int32_t* __restrict__ slot_of, int32_t* __restrict__ row_token,
+            const int32_t* __restrict__ offsets, int64_t Tu, int K, int E, int64_t C, const int64_t* __restrict__ cap_e,
+            int chunk_shift, int row_vecs, int64_t rows, int32_t* __restrict__ slot_of, int32_t* __restrict__ row_token,
             uint4* __restrict__ x_packed) {
   griddep_launch_dependents();
   griddep_wait();
@@ -200,7 +205,7 @@ pack_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ idx, const 
       const int pl = slot_of[u * K + lane];
       if (pl >= 0 && e >= 0 && e < E) {
         const int64_t place = (int64_t)chunk_base[(u >> chunk_shift) * E + e] + pl;
-        if (place < C) slot = offsets[e] + (int)place;
+        if (place < (cap_e ? cap_e[e] : C)) slot = offsets[e] + (int)place;
       }
       slot_of[u * K + lane] = slot;
       if (slot >= 0) row_token[slot] = (int32_t)u;
@@ -234,8 +239,8 @@ pack_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ idx, const 
 __global__ void __launch_bounds__(256)
 pack_bytes_kernel(const unsigned char* __restrict__ x, const int32_t* __restrict__ idx,
                   const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets, int64_t Tu, int K,
-                  int E, int64_t C, int chunk_shift, int64_t row_bytes, int64_t rows, int32_t* __restrict__ slot_of,
-                  int32_t* __restrict__ row_token, unsigned char* __restrict__ x_packed) {
+                  int E, int64_t C, const int64_t* __restrict__ cap_e, int chunk_shift, int64_t row_bytes, int64_t rows,
+                  int32_t* __restrict__ slot_of, int32_t* __restrict__ row_token, unsigned char* __restrict__ x_packed) {
   griddep_launch_dependents();
   griddep_wait();
   const int lane = threadIdx.x & 31;
@@ -247,7 +252,7 @@ pack_bytes_kernel(const unsigned char* __restrict__ x, const int32_t* __restrict
       const int pl = slot_of[u * K + lane];
       if (pl >= 0 && e >= 0 && e < E) {
         const int64_t place = (int64_t)chunk_base[(u >> chunk_shift) * E + e] + pl;
-        if (place < C) slot = offsets[e] + (int)place;
+        if (place < (cap_e ? cap_e[e] : C)) slot = offsets[e] + (int)place;
       }
       slot_of[u * K + lane] = slot;
       if (slot >= 0) row_token[slot] = (int32_t)u;
@@ -268,15 +273,15 @@ pack_bytes_kernel(const unsigned char* __restrict__ x, const int32_t* __restrict
 cudaError_t launch_scan(const Problem& p, int64_t nchunks, const int32_t* hist, const float* psum,
                         int32_t* chunk_base, int32_t* counts_ws, int32_t* offsets_ws, int32_t* counts_out,
                         int32_t* offsets_out, float* terms, unsigned int* ticket, float* aux_out, cudaStream_t s,
-                        bool pdl) {
+                        bool pdl, const int32_t* qbase, int64_t* cap_out) {
   return launch_kernel(scan_kernel, dim3((unsigned)p.E), dim3(kScanThreads), 0, s, 1, pdl, hist, nchunks, p.E, p.C,
                        psum, p.Tu, p.K, p.cfg.aux_alpha, chunk_base, counts_ws, offsets_ws, counts_out, offsets_out,
-                       terms, ticket, aux_out);
+                       terms, ticket, aux_out, qbase, cap_out);
 }
 
 cudaError_t launch_pack(const Problem& p, const void* x, const int32_t* idx, int chunk_shift, const int32_t* chunk_base,
                         const int32_t* offsets, int32_t* slot_of, int32_t* row_token, void* x_packed, cudaStream_t s,
-                        bool pdl) {
+                        bool pdl, const int64_t* cap_e) {
   const int64_t row_bytes = (int64_t)p.hu * (int64_t)p.elt;
   const int sms = device_sm_count();
   int64_t blocks = (p.Tu + 7) / 8;  // a warp per unit
@@ -286,11 +291,11 @@ cudaError_t launch_pack(const Problem& p, const void* x, const int32_t* idx, int
   if (row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
       (reinterpret_cast<uintptr_t>(x_packed) & 15) == 0)
     return launch_kernel(pack_kernel, dim3((unsigned)blocks), dim3(256), 0, s, 1, pdl, static_cast<const uint4*>(x),
-                         idx, chunk_base, offsets, p.Tu, p.K, p.E, p.C, chunk_shift, (int)(row_bytes / 16), p.rows,
+                         idx, chunk_base, offsets, p.Tu, p.K, p.E, p.C, cap_e, chunk_shift, (int)(row_bytes / 16), p.rows,
                          slot_of, row_token, static_cast<uint4*>(x_packed));
   return launch_kernel(pack_bytes_kernel, dim3((unsigned)blocks), dim3(256), 0, s, 1, pdl,
-                       static_cast<const unsigned char*>(x), idx, chunk_base, offsets, p.Tu, p.K, p.E, p.C, chunk_shift,
-                       row_bytes, p.rows, slot_of, row_token, static_cast<unsigned char*>(x_packed));
+                       static_cast<const unsigned char*>(x), idx, chunk_base, offsets, p.Tu, p.K, p.E, p.C, cap_e,
+                       chunk_shift, row_bytes, p.rows, slot_of, row_token, static_cast<unsigned char*>(x_packed));
 }
 
 cudaError_t launch_dispatch_from_idx(const Problem& p, const void* x, const int32_t* idx, int32_t* counts_out,
@@ -306,10 +311,11 @@ cudaError_t launch_dispatch_from_idx(const Problem& p, const void* x, const int3
     pdl = true;
   }
   e = launch_scan(p, nch, sc.chunk_hist, nullptr, sc.chunk_base, sc.counts, sc.offsets, counts_out, offsets_out,
-                  nullptr, sc.ticket, nullptr, s, pdl);
+                  nullptr, sc.ticket, nullptr, s, pdl, sc.qbase, sc.cap);
   if (e != cudaSuccess) return e;
   if (p.rows == 0) return cudaSuccess;
-  return launch_pack(p, x, idx, kChunkShift, sc.chunk_base, sc.offsets, slot_of, row_token, x_packed, s, true);
+  return launch_pack(p, x, idx, kChunkShift, sc.chunk_base, sc.offsets, slot_of, row_token, x_packed, s, true,
+                     sc.qbase ? sc.cap : nullptr);
 }
 
 }  // namespace moe

@@ -136,6 +136,7 @@ WsLayout ws_layout(const Problem& p) {
   L.chunk_base = take((size_t)p.ntiles * E * 4);
   L.psum = take((size_t)p.ntiles * E * 4);
   L.aux_terms = take(E * 4);
+  L.cap = take(E * 8);
   L.w_pad = take(p.bf16 ? (size_t)p.hu * ((E + 7) / 8 * 8) * 2 : 0);
   L.logits = take(p.bf16 ? 0 : (size_t)p.Tu * E * 4);
   L.rank = take(TK * 4);
@@ -337,6 +338,35 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
                                               (cudaStream_t)stream));
 }
 
+moe_status_t moe_dispatch_sharded(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
+                                  const int32_t* queue_base, int64_t T_global, int32_t* counts, int32_t* offsets,
+                                  int32_t* slot_of, int32_t* row_token, void* x_packed, void* ws, moe_stream_t stream) {
+  Problem p;
+  const moe_status_t st = make_problem(cfg, &p);
+  if (st != MOE_OK) return st;
+  if (!ws_ok(ws)) return MOE_ERR_WORKSPACE;
+  if (!offsets || !queue_base || T_global < cfg->T) return MOE_ERR_INVALID_ARG;
+  if (p.Tu > 0 && (!x || !topk_idx || !slot_of || !row_token || !x_packed)) return MOE_ERR_INVALID_ARG;
+  // the capacity of the whole batch: C = ceil(CF·K·T'_global/E)
+  moe_config_t g = *cfg;
+  g.T = T_global;
+  Problem pg;
+  if (make_problem(&g, &pg) != MOE_OK) return MOE_ERR_UNSUPPORTED;
+  p.C = pg.C;
+  const WsLayout L = ws_layout(p);
+  DispatchScratch sc;
+  sc.chunk_hist = ws_ptr<int32_t>(ws, L.chunk_hist);
+  sc.chunk_base = ws_ptr<int32_t>(ws, L.chunk_base);
+  sc.counts = ws_ptr<int32_t>(ws, L.counts);
+  sc.offsets = ws_ptr<int32_t>(ws, L.offsets);
+  sc.ticket = ws_ptr<unsigned int>(ws, L.status + 8);
+  sc.status = ws_ptr<uint32_t>(ws, L.status);
+  sc.qbase = queue_base;
+  sc.cap = ws_ptr<int64_t>(ws, L.cap);
+  return cuda_status(launch_dispatch_from_idx(p, x, topk_idx, counts, offsets, slot_of, row_token, x_packed, sc,
+                                              (cudaStream_t)stream));
+}
+
 moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_packed, const int32_t* offsets,
                             const void* w_gate, const void* w_up, const void* w_down,
                             void* y_packed, void* ws, moe_stream_t stream) {
@@ -372,14 +402,15 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* y_packed, const in
 // neighbouring stages are not overlapped by programmatic dependent launch).
 static constexpr int kForwardEvents = 6;
 
+// token_ids: null for the router, else the hash gate's token ids (K must be 1; no router weight).
 static moe_status_t forward_impl(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
                                  const moe_outputs_t* out, void* ws, moe_stream_t stream, void* gu,
-                                 void* const* events = nullptr) {
+                                 void* const* events = nullptr, const int32_t* token_ids = nullptr) {
   Problem p;
   const moe_status_t st = make_problem(cfg, &p);
   if (st != MOE_OK) return st;
   if (!ws_ok(ws)) return MOE_ERR_WORKSPACE;
-  if (!w || !w->w_router || !w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
+  if (!w || (!token_ids && !w->w_router) || !w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
   if (p.Tu > 0 && (!x || !y)) return MOE_ERR_INVALID_ARG;
   if (p.bf16 && !(aligned16(w->w_gate) && aligned16(w->w_up) && aligned16(w->w_down)))
     return MOE_ERR_INVALID_ARG;
@@ -405,11 +436,14 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const void* x, const m
   const bool pdl = events == nullptr;
   if (!mark(0)) return MOE_ERR_CUDA;
   // routing (each pick's place within its tile goes into slot_of, which the pack turns into slots)
-  cudaError_t e = route_stage(p, x, w->w_router, nullptr, w->logit_bias, w->select_bias, idx, gate, o.logits, slot_of,
-                              ws, s);
+  cudaError_t e = token_ids ? launch_hash_route(p, token_ids, idx, gate, slot_of, ws_ptr<int32_t>(ws, L.chunk_hist), s)
+                            : route_stage(p, x, w->w_router, nullptr, w->logit_bias, w->select_bias, idx, gate,
+                                          o.logits, slot_of, ws, s);
   if (e != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
-  // counts, offsets (into the workspace; the caller's copies are optional) and the aux loss
-  e = scan_stage(p, ws, o.counts, o.offsets, o.aux, s, pdl);
+  // counts, offsets (into the workspace; the caller's copies are optional) and the aux loss (the
+  // hash gate has no routing probabilities, so no aux loss: 0)
+  if (token_ids && o.aux && cudaMemsetAsync(o.aux, 0, sizeof(float), s) != cudaSuccess) return MOE_ERR_CUDA;
+  e = scan_stage(p, ws, o.counts, o.offsets, token_ids ? nullptr : o.aux, s, pdl && !token_ids);
   if (e != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
   if (p.rows > 0) {
     e = launch_pack(p, x, idx, kTileShift, ws_ptr<int32_t>(ws, L.chunk_base), offsets_ws, slot_of, row_token, x_packed,
@@ -436,6 +470,30 @@ moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x, const 
   for (int i = 0; i < kForwardEvents; ++i)
     if (!events[i]) return MOE_ERR_INVALID_ARG;
   return forward_impl(cfg, x, w, y, out, ws, stream, nullptr, events);
+}
+
+moe_status_t moe_route_hash(const moe_config_t* cfg, const int32_t* token_ids, int32_t* topk_idx, float* topk_gate,
+                            void* ws, moe_stream_t stream) {
+  Problem p;
+  const moe_status_t st = make_problem(cfg, &p);
+  if (st != MOE_OK) return st;
+  if (p.K != 1) return MOE_ERR_UNSUPPORTED;
+  if (!ws_ok(ws)) return MOE_ERR_WORKSPACE;
+  if (p.Tu > 0 && (!token_ids || !topk_idx || !topk_gate)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(p);
+  return cuda_status(launch_hash_route(p, token_ids, topk_idx, topk_gate, ws_ptr<int32_t>(ws, L.rank),
+                                       ws_ptr<int32_t>(ws, L.chunk_hist), (cudaStream_t)stream));
+}
+
+moe_status_t moe_forward_hash(const moe_config_t* cfg, const void* x, const int32_t* token_ids, const moe_weights_t* w,
+                              void* y, const moe_outputs_t* out, void* ws, moe_stream_t stream) {
+  Problem p;
+  const moe_status_t st = make_problem(cfg, &p);
+  if (st != MOE_OK) return st;
+  if (p.K != 1) return MOE_ERR_UNSUPPORTED;
+  if (p.Tu > 0 && !token_ids) return MOE_ERR_INVALID_ARG;
+  static const int32_t kNoUnits = 0;  // T' = 0: any non-null pointer selects the hash gate
+  return forward_impl(cfg, x, w, y, out, ws, stream, nullptr, nullptr, token_ids ? token_ids : &kNoUnits);
 }
 
 size_t moe_saved_gu_size(const moe_config_t* cfg) {

@@ -60,6 +60,7 @@ struct WsLayout {
   size_t chunk_base;   // int32 [ntiles][E] each tile's / chunk's base in the expert queues
   size_t psum;         // float [ntiles][E] Σ over the tile's units of p_{t,e}
   size_t aux_terms;    // float [E] per-expert aux terms
+  size_t cap;          // int64 [E] capacity left per expert (dispatch of a shard)
   size_t w_pad;        // bf16 [h'][E rounded up to 8] router weight copy (bf16 layers, when needed)
   size_t logits;       // float [T'][E] router logits (fp32 layers)
   size_t rank;         // int32 [T'][K] pick places within their tile (routing calls alone)
@@ -82,6 +83,8 @@ struct DispatchScratch {
   int32_t* offsets;      // [E+1]
   unsigned int* ticket;  // zero between calls
   uint32_t* status;      // or null
+  const int32_t* qbase = nullptr;  // shard of a larger batch: picks per expert on earlier ranks [E]
+  int64_t* cap = nullptr;          // then: capacity left per expert [E] (scratch)
 };
 
 moe_status_t make_problem(const moe_config_t* cfg, Problem* p);
@@ -159,16 +162,19 @@ cudaError_t launch_router_simt_logits(const Problem& p, const void* x, const voi
 cudaError_t launch_select_logits(const Problem& p, const float* logits, const float* logit_bias, const SelectCtx& sel,
                                  float* logits_out, int32_t* rank_out, int32_t* tile_hist, float* tile_psum,
                                  cudaStream_t s, bool pdl);
+// Hash gate (K = 1): expert fmix32(token id) mod E, gate 1, with the per-tile counts and places.
+cudaError_t launch_hash_route(const Problem& p, const int32_t* token_ids, int32_t* idx, float* gate, int32_t* rank_out,
+                              int32_t* tile_hist, cudaStream_t s);
 // Per expert: chunk bases, pre-drop counts, offsets; the aux loss when psum and aux_out are given.
 cudaError_t launch_scan(const Problem& p, int64_t nchunks, const int32_t* hist, const float* psum,
                         int32_t* chunk_base, int32_t* counts_ws, int32_t* offsets_ws, int32_t* counts_out,
                         int32_t* offsets_out, float* terms, unsigned int* ticket, float* aux_out, cudaStream_t s,
-                        bool pdl);
+                        bool pdl, const int32_t* qbase = nullptr, int64_t* cap_out = nullptr);
 // Slots of the picks (slot_of holds the places within chunks of 2^chunk_shift units on entry) and
 // the packed rows.
 cudaError_t launch_pack(const Problem& p, const void* x, const int32_t* idx, int chunk_shift, const int32_t* chunk_base,
                         const int32_t* offsets, int32_t* slot_of, int32_t* row_token, void* x_packed, cudaStream_t s,
-                        bool pdl);
+                        bool pdl, const int64_t* cap_e = nullptr);
 // The whole dispatch from given picks: chunk ranks, scan, pack.
 cudaError_t launch_dispatch_from_idx(const Problem& p, const void* x, const int32_t* idx, int32_t* counts_out,
                                      int32_t* offsets_out, int32_t* slot_of, int32_t* row_token, void* x_packed,

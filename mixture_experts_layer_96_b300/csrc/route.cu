@@ -308,7 +308,52 @@ static cudaError_t launch_router_simt(const Problem& p, const void* x, const voi
   }
 }
 
+// MurmurHash3's 32-bit finalizer (xor-shift 16, ·0x85ebca6b, xor-shift 13, ·0xc2b2ae35, xor-shift 16).
+__device__ __forceinline__ uint32_t fmix32(uint32_t h) {
+  h ^= h >> 16;
+  h *= 0x85ebca6bu;
+  h ^= h >> 13;
+  h *= 0xc2b2ae35u;
+  h ^= h >> 16;
+  return h;
+}
+
+// Hash gate: unit u goes to expert fmix32(token_ids[u]) mod E with gate 1 (top-1). A block per
+// 128-unit tile also leaves the tile's picks per expert and each pick's place among them, as the
+// router kernels do, for the scan and pack.
+__global__ void __launch_bounds__(kTileUnits)
+hash_route_kernel(const int32_t* __restrict__ ids, int64_t Tu, int E, int32_t* __restrict__ idx,
+                  float* __restrict__ gate, int32_t* __restrict__ rank_out, int32_t* __restrict__ tile_hist) {
+  __shared__ int picks[kTileUnits * kPickStride];
+  __shared__ int rank[kTileUnits * kPickStride];
+  __shared__ uint32_t lanes_of[(kTileUnits / 32) * kMaxExperts];
+  __shared__ int warp_pre[(kTileUnits / 32) * kMaxExperts];
+  __shared__ int hist[kMaxExperts];
+  griddep_launch_dependents();
+  griddep_wait();
+  const int t = threadIdx.x;
+  const int64_t u0 = (int64_t)blockIdx.x * kTileUnits, u = u0 + t;
+  const int R = (int)min((int64_t)kTileUnits, Tu - u0);
+  if (t < R) {
+    const int e = (int)(fmix32((uint32_t)ids[u]) % (uint32_t)E);
+    idx[u] = e;
+    gate[u] = 1.0f;
+    picks[t * kPickStride] = e;
+  }
+  __syncthreads();
+  rank_picks(picks, R, 1, E, rank, hist, lanes_of, warp_pre);
+  if (t < R) rank_out[u] = rank[t * kPickStride];
+  for (int e = t; e < E; e += kTileUnits) tile_hist[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
 }  // namespace
+
+cudaError_t launch_hash_route(const Problem& p, const int32_t* token_ids, int32_t* idx, float* gate, int32_t* rank_out,
+                              int32_t* tile_hist, cudaStream_t s) {
+  if (p.Tu == 0) return cudaSuccess;
+  return launch_kernel(hash_route_kernel, dim3((unsigned)p.ntiles), dim3(kTileUnits), 0, s, 1, false, token_ids, p.Tu,
+                       p.E, idx, gate, rank_out, tile_hist);
+}
 
 cudaError_t launch_select_logits(const Problem& p, const float* logits, const float* logit_bias, const SelectCtx& sel,
                                  float* logits_out, int32_t* rank_out, int32_t* tile_hist, float* tile_psum,

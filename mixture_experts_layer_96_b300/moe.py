@@ -26,7 +26,7 @@ EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_capacity", "moe_rout
            "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_status",
            "moe_status_string", "moe_launch_count", "moe_abi_version", "moe_dispatch_noalloc",
            "moe_saved_gu_size", "moe_forward_train", "moe_backward_workspace_size", "moe_backward",
-           "moe_forward_profiled")
+           "moe_forward_profiled", "moe_route_hash", "moe_forward_hash", "moe_dispatch_sharded")
 
 
 class MoEError(RuntimeError):
@@ -95,6 +95,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_expert_ffn": (I32, [cfgp, P, P, P, P, P, P, P, P]),
         "moe_combine": (I32, [cfgp, P, P, P, P, P, P]),
         "moe_forward": (I32, [cfgp, P, ctypes.POINTER(MoEWeights), P, ctypes.POINTER(MoEOutputs), P, P]),
+        "moe_route_hash": (I32, [cfgp, P, P, P, P, P]),
+        "moe_dispatch_sharded": (I32, [cfgp, P, P, P, I64, P, P, P, P, P, P, P]),
+        "moe_forward_hash": (I32, [cfgp, P, P, ctypes.POINTER(MoEWeights), P, ctypes.POINTER(MoEOutputs), P, P]),
         "moe_forward_profiled": (I32, [cfgp, P, ctypes.POINTER(MoEWeights), P, ctypes.POINTER(MoEOutputs), P,
                                        ctypes.POINTER(ctypes.c_void_p), P]),
         "moe_get_status": (I32, [P, P]),
@@ -304,6 +307,29 @@ def moe_dispatch(cfg: MoEConfig, x, topk_idx, *, ws: Workspace, counts=None, off
     return counts, offsets, slot_of, row_token, x_packed
 
 
+def moe_dispatch_sharded(cfg: MoEConfig, x, topk_idx, queue_base, T_global: int, *, ws: Workspace, counts=None,
+                         offsets=None, slot_of=None, row_token=None, x_packed=None, stream=None):
+    """Dispatch of one token shard of a batch of T_global tokens: queue_base [E] int32 holds each
+    expert's picks on the earlier shards; capacity and drop order are the whole batch's.
+    Returns (counts, offsets, slot_of, row_token, x_packed), local to the shard."""
+    lib = load_library()
+    dt, dev = cfg.torch_dtype, x.device
+    Tu, hu, E, K = cfg.T_units, cfg.h_unit, cfg.E, cfg.K
+    _req(x, "x", (cfg.T, cfg.h), dt)
+    _req(topk_idx, "topk_idx", (Tu, K), torch.int32)
+    _req(queue_base, "queue_base", (E,), torch.int32)
+    counts = counts if counts is not None else torch.empty((E,), dtype=torch.int32, device=dev)
+    offsets = offsets if offsets is not None else torch.empty((E + 1,), dtype=torch.int32, device=dev)
+    slot_of = slot_of if slot_of is not None else torch.empty((Tu, K), dtype=torch.int32, device=dev)
+    row_token = row_token if row_token is not None else torch.empty((Tu * K,), dtype=torch.int32, device=dev)
+    x_packed = x_packed if x_packed is not None else torch.empty((Tu * K, hu), dtype=dt, device=dev)
+    _check(_run([x, topk_idx, queue_base, counts, offsets, slot_of, row_token, x_packed, ws.buf], stream,
+                lib.moe_dispatch_sharded, ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(queue_base),
+                ctypes.c_int64(T_global), _ptr(counts), _ptr(offsets), _ptr(slot_of), _ptr(row_token),
+                _ptr(x_packed), ws.ptr), "moe_dispatch_sharded")
+    return counts, offsets, slot_of, row_token, x_packed
+
+
 def moe_expert_ffn(cfg: MoEConfig, x_packed, offsets, w_gate, w_up, w_down, *, ws: Workspace,
                    y_packed=None, stream=None):
     """Per-expert SwiGLU FFN over packed rows. Returns y_packed [T'K][h']."""
@@ -411,6 +437,41 @@ def moe_forward(cfg: MoEConfig, x, weights: LayerWeights, *, ws: Workspace, y=No
     _check(_run([x, y, ws.buf, *weights.tensors(), *(outputs.tensors() if outputs is not None else ())], stream,
                 lib.moe_forward, ctypes.byref(cfg), _ptr(x), ctypes.byref(cw), _ptr(y),
                 ctypes.byref(co) if co is not None else None, ws.ptr), "moe_forward")
+    return y
+
+
+def moe_route_hash(cfg: MoEConfig, token_ids, *, ws: Workspace, topk_idx=None, topk_gate=None, stream=None):
+    """Hash gate (top-1): expert fmix32(token id) mod E, gate 1. token_ids [T'] int32.
+    Returns (topk_idx [T'][1], topk_gate [T'][1])."""
+    lib = load_library()
+    Tu, dev = cfg.T_units, token_ids.device
+    _req(token_ids, "token_ids", (Tu,), torch.int32)
+    topk_idx = topk_idx if topk_idx is not None else torch.empty((Tu, cfg.K), dtype=torch.int32, device=dev)
+    topk_gate = topk_gate if topk_gate is not None else torch.empty((Tu, cfg.K), dtype=torch.float32, device=dev)
+    _req(topk_idx, "topk_idx", (Tu, cfg.K), torch.int32)
+    _req(topk_gate, "topk_gate", (Tu, cfg.K), torch.float32)
+    _check(_run([token_ids, topk_idx, topk_gate, ws.buf], stream, lib.moe_route_hash, ctypes.byref(cfg),
+                _ptr(token_ids), _ptr(topk_idx), _ptr(topk_gate), ws.ptr), "moe_route_hash")
+    return topk_idx, topk_gate
+
+
+def moe_forward_hash(cfg: MoEConfig, x, token_ids, w_gate, w_up, w_down, *, ws: Workspace, y=None,
+                     outputs: Optional[ForwardOutputs] = None, stream=None):
+    """The layer with the hash gate: x [T][h], token_ids [T'] int32 → y [T][h]. Returns y."""
+    lib = load_library()
+    dt, hu, E, F = cfg.torch_dtype, cfg.h_unit, cfg.E, cfg.d_ff
+    _req(x, "x", (cfg.T, cfg.h), dt)
+    _req(token_ids, "token_ids", (cfg.T_units,), torch.int32)
+    _req(w_gate, "w_gate", (E, F, hu), dt)
+    _req(w_up, "w_up", (E, F, hu), dt)
+    _req(w_down, "w_down", (E, hu, F), dt)
+    y = y if y is not None else torch.empty((cfg.T, cfg.h), dtype=dt, device=x.device)
+    _req(y, "y", (cfg.T, cfg.h), dt)
+    cw = MoEWeights(None, None, None, _ptr(w_gate), _ptr(w_up), _ptr(w_down))
+    co = outputs.c_struct() if outputs is not None else None
+    _check(_run([x, token_ids, y, w_gate, w_up, w_down, ws.buf, *(outputs.tensors() if outputs is not None else ())],
+                stream, lib.moe_forward_hash, ctypes.byref(cfg), _ptr(x), _ptr(token_ids), ctypes.byref(cw), _ptr(y),
+                ctypes.byref(co) if co is not None else None, ws.ptr), "moe_forward_hash")
     return y
 
 

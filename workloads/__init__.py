@@ -271,6 +271,12 @@ class Generator:
         g = np.random.default_rng([self.seed, 100, 0, 0])
         return (g.standard_normal((s.T_units, s.E), dtype=np.float32) * np.float32(scale))
 
+    def token_ids(self, vocab: int = 32000) -> np.ndarray:
+        """Seeded token ids [T'] int32, uniform in [0, vocab) (the hash gate's input)."""
+        s = self.shape
+        g = np.random.default_rng([self.seed, 103, 0, 0])
+        return g.integers(0, vocab, size=s.T_units, dtype=np.int64).astype(np.int32)
+
     def topk_idx(self) -> np.ndarray:
         """Seeded routing decisions [T'][K] int32 (K distinct experts per unit, Zipf-skewed),
         for dispatch-stage checks."""
