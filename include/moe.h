@@ -176,7 +176,11 @@ MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const void* y_packed, 
                          const float* topk_gate, void* y, void* ws, moe_stream_t stream);
 
 /* The whole layer: route → dispatch → expert FFN → combine (+ aux). x [T][h] → y [T][h].
- * `out` may be NULL or have NULL members; intermediates live in `ws`. */
+ * `out` may be NULL or have NULL members; intermediates live in `ws`.
+ * With K == 1 (bf16, 16-byte aligned y) the combine is folded into the down GEMM: each kept row
+ * writes g·Y straight into y, with moe_combine's arithmetic, so y has the same bits as
+ * route → dispatch → expert_ffn → combine; y_packed is then not written (moe_forward_train still
+ * writes it). moe_set_expert_gemm can fold it for K >= 2 as well, or not at all. */
 MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y,
                          const moe_outputs_t* out, void* ws, moe_stream_t stream);
 
@@ -201,7 +205,8 @@ MOE_API moe_status_t moe_forward_hash(const moe_config_t* cfg, const void* x, co
 /* moe_forward with a CUDA event recorded on `stream` at each boundary between its stages, for
  * timing them (instrumentation; the pages have no counterpart). events: 6 caller-created cudaEvent_t
  * (as void*), recorded before the routing, after the routing, after the scan (counts, offsets, aux
- * loss), after the pack, after the expert GEMMs and after the combine. The kernels are the same as
+ * loss), after the pack, after the expert GEMMs and after the combine (recorded right after the
+ * GEMMs where the combine is folded into the down GEMM). The kernels are the same as
  * moe_forward's, but neighbouring stages no longer overlap their launch (programmatic dependent
  * launch is off), so the sum of the stage times can exceed a moe_forward call's time.
  * MOE_ERR_INVALID_ARG if events or one of them is NULL. */
@@ -267,6 +272,20 @@ MOE_API uint64_t moe_launch_count(void);
 
 /* MOE_ABI_VERSION of the loaded library. */
 MOE_API int32_t moe_abi_version(void);
+
+/* Choices of the tensor-core expert GEMMs, process-wide, for tests and tuning (the pages have no
+ * counterpart). Each is 1 (on), 0 (off) or -1 (automatic).
+ *  pair_tiles: CTA-pair 256-row tiles instead of single-CTA 128-row tiles; automatic: when the
+ *    packed rows average at least 256 per expert.
+ *  transposed_tails: pair-tile tails of up to 224 rows run transposed; automatic: when the
+ *    reduction has at least 16 k-blocks of 64.
+ *  fold_combine: moe_forward folds the combine into the down GEMM (bf16, 16-byte aligned y);
+ *    automatic: when K == 1, where each unit's one kept row writes g·Y straight into y. With K >= 2
+ *    the last row of each unit sums it (arrival counters per 32 columns), which costs the down GEMM
+ *    more than the separate combine launch on the measured layers.
+ * Takes effect at the next launch; y has the same bits either way. MOE_ERR_INVALID_ARG for other
+ * values. Host only. */
+MOE_API moe_status_t moe_set_expert_gemm(int32_t pair_tiles, int32_t transposed_tails, int32_t fold_combine);
 
 /* Dispatch for callers that cannot allocate device memory. (The pages have no counterpart of this
  * call; it exists for how the library is deployed, not for the method.)

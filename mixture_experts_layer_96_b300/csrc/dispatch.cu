@@ -193,7 +193,8 @@ __global__ void __launch_bounds__(256)
 pack_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ idx, const int32_t* __restrict__ chunk_base,
             const int32_t* __restrict__ offsets, int64_t Tu, int K, int E, int64_t C, const int64_t* __restrict__ cap_e,
             int chunk_shift, int row_vecs, int64_t rows, int32_t* __restrict__ slot_of, int32_t* __restrict__ row_token,
-            uint4* __restrict__ x_packed) {
+            uint4* __restrict__ x_packed, uint4* __restrict__ y_zero, uint32_t* __restrict__ arrivals,
+            int arrivals_per_unit) {
   griddep_launch_dependents();
   griddep_wait();
   const int lane = threadIdx.x & 31;
@@ -210,6 +211,12 @@ pack_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ idx, const 
       slot_of[u * K + lane] = slot;
       if (slot >= 0) row_token[slot] = (int32_t)u;
     }
+    // combine folded into the down GEMM: its arrival counters start at zero, and a unit none of
+    // whose picks was kept gets y = 0 here (no GEMM row writes it)
+    if (arrivals != nullptr)
+      for (int i = lane; i < arrivals_per_unit; i += 32) arrivals[u * arrivals_per_unit + i] = 0u;
+    if (y_zero != nullptr && __ballot_sync(0xffffffffu, slot >= 0) == 0u)
+      for (int v = lane; v < row_vecs; v += 32) y_zero[u * row_vecs + v] = make_uint4(0u, 0u, 0u, 0u);
     const uint4* src = x + u * row_vecs;
     for (int v0 = 0; v0 < row_vecs; v0 += 32 * 8) {
       uint4 buf[8];
@@ -281,18 +288,21 @@ cudaError_t launch_scan(const Problem& p, int64_t nchunks, const int32_t* hist, 
 
 cudaError_t launch_pack(const Problem& p, const void* x, const int32_t* idx, int chunk_shift, const int32_t* chunk_base,
                         const int32_t* offsets, int32_t* slot_of, int32_t* row_token, void* x_packed, cudaStream_t s,
-                        bool pdl, const int64_t* cap_e) {
+                        bool pdl, const int64_t* cap_e, void* y_zero, uint32_t* arrivals) {
   const int64_t row_bytes = (int64_t)p.hu * (int64_t)p.elt;
   const int sms = device_sm_count();
   int64_t blocks = (p.Tu + 7) / 8;  // a warp per unit
   if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
   const int64_t tail_blocks = (p.rows + 255) / 256;
   if (blocks < 1) blocks = tail_blocks < 1 ? 1 : (tail_blocks < sms ? tail_blocks : sms);
-  if (row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
-      (reinterpret_cast<uintptr_t>(x_packed) & 15) == 0)
+  const bool vec = row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(x_packed) & 15) == 0;
+  if (vec && (reinterpret_cast<uintptr_t>(y_zero) & 15) == 0)
     return launch_kernel(pack_kernel, dim3((unsigned)blocks), dim3(256), 0, s, 1, pdl, static_cast<const uint4*>(x),
                          idx, chunk_base, offsets, p.Tu, p.K, p.E, p.C, cap_e, chunk_shift, (int)(row_bytes / 16), p.rows,
-                         slot_of, row_token, static_cast<uint4*>(x_packed));
+                         slot_of, row_token, static_cast<uint4*>(x_packed), static_cast<uint4*>(y_zero), arrivals,
+                         p.hu / 32);
+  if (y_zero != nullptr || arrivals != nullptr) return cudaErrorInvalidValue;  // only the vector pack prepares the folded combine
   return launch_kernel(pack_bytes_kernel, dim3((unsigned)blocks), dim3(256), 0, s, 1, pdl,
                        static_cast<const unsigned char*>(x), idx, chunk_base, offsets, p.Tu, p.K, p.E, p.C, cap_e,
                        chunk_shift, row_bytes, p.rows, slot_of, row_token, static_cast<unsigned char*>(x_packed));

@@ -13,7 +13,7 @@
 // Tiles run expert by expert, n-tile by n-tile, with the m-tiles of an expert adjacent so the
 // CTAs working at the same time share each weight tile through L2. The schedule comes from the
 // device-side offsets: no host sync between dispatch and this kernel. Every wait is bounded.
-#include <stdlib.h>
+#include <atomic>
 
 #include "moe_device.cuh"
 #include "moe_internal.h"
@@ -43,6 +43,15 @@ struct TcParams {
   uint32_t* status;
   int swap_max;            // pair tiles: last m-tiles of at most this many rows run transposed (0: none)
   __nv_bfloat16* save_gu;  // gate/up: G | U pre-activations [rows][2·n_out] (bf16) when not null
+  // down GEMM with the combine folded in (kernels instantiated with FK > 0)
+  __nv_bfloat16* y;            // [T'][n_out] layer output
+  const int32_t* row_token;    // [rows] packed row -> unit
+  const int32_t* slot_of;      // [T'][topk] packed row of each pick, -1: dropped
+  const float* gate;           // [T'][topk]
+  uint32_t* arrivals;          // [T'][n_out/32] rows of the unit done per 32-column chunk, zero on entry
+  int64_t Tu;
+  int topk;
+  int keep_packed;             // write every Y row to out (the backward reads Y_packed)
 };
 
 // 32 fp32 values (as bits) → 32 bf16 at dst (64 bytes, 16-byte aligned).
@@ -56,7 +65,187 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t
                        pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
 }
 
-template <int EPI>
+// ------------------------------------------------------------------------------------------------
+// Combine folded into the down GEMM's epilogue.
+//   [Lesson 10 "专家并行 EP", §1: y = Σ_{i∈TopK} s_i(x)·FFN_i(x); §3 steps 3-4: each result goes
+//    back to its unit and the unit's results are summed with the gates kept from routing]
+// A unit with one kept pick is finished by that pick's row: the epilogue writes g·Y into y. A unit
+// with k >= 2 kept picks is finished, per 32-column chunk, by whichever of its rows gets there last:
+// every row writes its Y chunk to Y_packed, makes it visible (__threadfence) and adds one to the
+// chunk's arrival counter; the row that reads k - 1 back loads the unit's k chunks (L2, bypassing
+// L1) and writes y = Σ_k g_k·Y_k with the separate combine's arithmetic: the same fp32 fmaf chain in
+// k order from +0, dropped picks adding 0·0. The result is therefore bit-identical to the two-launch
+// path and independent of the order in which rows arrive. The pack zeroes the counters and the y
+// rows of units whose picks were all dropped.
+
+// What a lane knows about the unit of the packed row (or token) it owns.
+template <int FK>
+struct CombineRow {
+  int t;           // unit, -1: this lane owns none
+  int kept;        // kept picks of the unit
+  int own;         // pick index of the owned row
+  int32_t sl[FK];  // packed rows of the unit's picks (-1: dropped or k >= topk)
+  float g[FK];     // their gates (0 where sl is -1)
+};
+
+template <int FK>
+__device__ __forceinline__ void combine_row_clear(CombineRow<FK>& c) {
+  c.t = -1;
+  c.kept = 0;
+  c.own = -1;
+#pragma unroll
+  for (int k = 0; k < FK; ++k) {
+    c.sl[k] = -1;
+    c.g[k] = 0.f;
+  }
+}
+
+template <int FK>
+__device__ __forceinline__ void combine_row_load(const TcParams& p, int64_t slot, CombineRow<FK>& c) {
+  combine_row_clear(c);
+  const int t = __ldg(p.row_token + slot);
+  if (t < 0 || (int64_t)t >= p.Tu) {
+    set_status(p.status, kDevErrBadIndex);
+    return;
+  }
+  int own = -1, kept = 0;
+#pragma unroll
+  for (int k = 0; k < FK; ++k) {
+    if (k < p.topk) {
+      int s = __ldg(p.slot_of + (int64_t)t * p.topk + k);
+      if ((int64_t)s >= p.rows_cap) {
+        set_status(p.status, kDevErrBadIndex);
+        s = -1;
+      }
+      if (s >= 0) {
+        c.sl[k] = s;
+        c.g[k] = __ldg(p.gate + (int64_t)t * p.topk + k);
+        ++kept;
+        if ((int64_t)s == slot) own = k;
+      }
+    }
+  }
+  if (own < 0) {  // the row is not among its unit's picks
+    set_status(p.status, kDevErrBadIndex);
+    combine_row_clear(c);
+    return;
+  }
+  c.t = t;
+  c.kept = kept;
+  c.own = own;
+}
+
+__device__ __forceinline__ uint4 ld_global_cg_v4(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
+
+// Count the owned row into the arrival counters of its chunks (bit c of `chunks`: counter
+// base[c]); returns the chunks this row completes. The caller's Y stores precede it.
+template <int FK>
+__device__ __forceinline__ uint32_t combine_arrive(const TcParams& p, const CombineRow<FK>& c, uint32_t* base,
+                                                   uint32_t chunks) {
+  if (c.t < 0) return 0u;
+  if (c.kept == 1) return chunks;
+  __threadfence();  // this row's Y chunks are visible before it is counted
+  uint32_t last = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if ((chunks >> i) & 1u) {
+      const uint32_t old = atomicAdd(base + i, 1u);
+      if (old + 1u == (uint32_t)c.kept) last |= 1u << i;
+      else if (old >= (uint32_t)c.kept) set_status(p.status, kDevErrBadIndex);
+    }
+  }
+  if (last) __threadfence();  // the other rows' chunks are read after their counts were seen
+  return last;
+}
+
+// y chunks of the units whose last rows are held by lanes with last != 0 (bit c: 32-column chunk c
+// from col0). LPO lanes serve one owner, 16 bytes (8 columns) each: LPO = 32 covers 256 columns
+// (a row of a 128 x 256 tile), LPO = 4 covers 32 (a transposed tile's warp). R batches of 32/LPO
+// owners are loaded before any is summed. The whole warp calls this.
+template <int FK, int LPO>
+__device__ __forceinline__ void combine_owned(const TcParams& p, uint32_t last, const CombineRow<FK>& c, int col0) {
+  constexpr int OPP = 32 / LPO;
+  constexpr int R = FK <= 2 ? 8 : 2;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % LPO, pos = lane / LPO;
+  const int col = col0 + sub * 8;
+  uint32_t owners = __ballot_sync(0xffffffffu, last != 0u);
+  while (owners != 0u) {
+    uint4 raw[R][FK];
+    float gw[R][FK];
+    int64_t dst[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const uint32_t o = __fns(owners, 0, r * OPP + pos + 1);
+      const int src = o < 32u ? (int)o : lane;
+      const int t = __shfl_sync(0xffffffffu, c.t, src);
+      const uint32_t m = __shfl_sync(0xffffffffu, last, src);
+      const bool ok = o < 32u && ((m >> (sub >> 2)) & 1u) != 0u && col < p.n_out;
+      dst[r] = ok ? (int64_t)t * p.n_out + col : -1;
+#pragma unroll
+      for (int k = 0; k < FK; ++k) {
+        const int s = __shfl_sync(0xffffffffu, c.sl[k], src);
+        gw[r][k] = __shfl_sync(0xffffffffu, c.g[k], src);
+        raw[r][k] = make_uint4(0u, 0u, 0u, 0u);
+        if (ok && s >= 0) raw[r][k] = ld_global_cg_v4(p.out + (int64_t)s * p.n_out + col);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (dst[r] < 0) continue;
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+#pragma unroll
+      for (int k = 0; k < FK; ++k) {
+        if (k < p.topk) {
+          const __nv_bfloat16* pv = reinterpret_cast<const __nv_bfloat16*>(&raw[r][k]);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = fmaf(gw[r][k], __bfloat162float(pv[q]), acc[q]);
+        }
+      }
+      *reinterpret_cast<uint4*>(p.y + dst[r]) =
+          make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                     pack_bf16x2(acc[6], acc[7]));
+    }
+#pragma unroll 1
+    for (int i = 0; i < R * OPP && owners != 0u; ++i) owners &= owners - 1u;
+  }
+}
+
+// g·Y of a unit with one kept pick (pick `own` of topk), 32 columns: the separate combine's chain
+// (fp32 fmaf in k order from +0, dropped picks adding 0·0) with Y rounded to bf16 first.
+template <int FK>
+__device__ __forceinline__ void store_direct_x32(const TcParams& p, const CombineRow<FK>& c, __nv_bfloat16* dst,
+                                                 const uint32_t (&pk)[16]) {
+  uint32_t o[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&pk[j]);
+    const float v0 = __low2float(v2), v1 = __high2float(v2);
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < FK; ++k) {
+      if (k < p.topk) {
+        const bool mine = k == c.own;
+        a0 = fmaf(c.g[k], mine ? v0 : 0.f, a0);
+        a1 = fmaf(c.g[k], mine ? v1 : 0.f, a1);
+      }
+    }
+    o[j] = pack_bf16x2(a0, a1);
+  }
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+}
+
+template <int EPI, int FK>
 __global__ void __launch_bounds__(kTcThreads, 1)
 expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                       const __grid_constant__ CUtensorMap tmB1, TcParams p) {
@@ -201,14 +390,19 @@ expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       decode_tile(tile, s_pre, p.E, p.n_tiles, e, mt, nt);
       const int acc = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+      const int rows_e = s_off[e + 1] - s_off[e];
+      const int r_local = mt * kBM + q * 32 + lane;
+      const bool row_ok = r_local < rows_e;
+      CombineRow<(FK > 0 ? FK : 1)> cr;
+      if constexpr (FK > 0) {  // the row's unit, read while the MMAs run
+        if (row_ok) combine_row_load(p, (int64_t)s_off[e] + r_local, cr);
+        else combine_row_clear(cr);
+      }
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) {
         if (lane == 0) { s_abort = 1; set_status(p.status, kDevErrTimeout); }
         break;
       }
       tc_fence_after();
-      const int rows_e = s_off[e + 1] - s_off[e];
-      const int r_local = mt * kBM + q * 32 + lane;
-      const bool row_ok = r_local < rows_e;
       __nv_bfloat16* orow = p.out + (int64_t)(s_off[e] + r_local) * p.n_out;
       const uint32_t t_row = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(q * 32) << 16);
       if (EPI == kEpiSwiGLU) {
@@ -248,15 +442,32 @@ expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-            uint4* dst = reinterpret_cast<uint4*>(orow + col);
+            const bool direct = FK > 0 && cr.kept == 1;
+            if (!direct || p.keep_packed) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + col);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+              for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
+            if constexpr (FK > 0) {
+              if (direct) store_direct_x32(p, cr, p.y + (int64_t)cr.t * p.n_out + col, pk);
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if constexpr (FK > 0) {
+        // the accumulator is free again; finish the units whose last row this was
+        uint32_t chunks = 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          if (nt * kBN + c * 32 < p.n_out) chunks |= 1u << c;
+        const uint32_t last =
+            cr.kept >= 2 ? combine_arrive(p, cr, p.arrivals + (int64_t)cr.t * (p.n_out >> 5) + nt * (kBN / 32), chunks)
+                         : 0u;
+        combine_owned<FK, 32>(p, last, cr, nt * kBN);
+      }
     }
   }
 
@@ -307,7 +518,7 @@ constexpr int kSwapHalf = 64;       // W1 (then W3) rows per CTA in a swapped ga
 // Tokens per CTA in a swapped tail tile of `tail` rows (N = twice this, a multiple of 16).
 __device__ __forceinline__ int swap_half_n(int tail) { return ((tail + 15) & ~15) >> 1; }
 
-template <int EPI>
+template <int EPI, int FK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
 expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                            const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmS0,
@@ -493,15 +704,20 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
       decode_tile(tile, s_pre, p.E, p.n_tiles, e, mt, nt);
       const int acc = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+      const int rows_e = s_off[e + 1] - s_off[e];
+      const int tail = rows_e - mt * kPairBM;
+      const int r_local = mt * kPairBM + (int)rank * 128 + q * 32 + lane;
+      const bool row_ok = r_local < rows_e;
+      CombineRow<(FK > 0 ? FK : 1)> cr;
+      if constexpr (FK > 0) {  // the row's unit (plain tiles), read while the MMAs run
+        if (row_ok && tail > p.swap_max) combine_row_load(p, (int64_t)s_off[e] + r_local, cr);
+        else combine_row_clear(cr);
+      }
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) {
         if (lane == 0) abort_both();
         break;
       }
       tc_fence_after();
-      const int rows_e = s_off[e + 1] - s_off[e];
-      const int tail = rows_e - mt * kPairBM;
-      const int r_local = mt * kPairBM + (int)rank * 128 + q * 32 + lane;
-      const bool row_ok = r_local < rows_e;
       __nv_bfloat16* orow = p.out + (int64_t)(s_off[e] + r_local) * p.n_out;
       const uint32_t t_row = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(q * 32) << 16);
       if (tail <= p.swap_max) {
@@ -584,6 +800,12 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
           const bool cols_ok = col0 < p.n_out;
 #pragma unroll 1
           for (int c0 = 0; c0 < n_tok; c0 += 32) {
+            if constexpr (FK > 0) {  // lane owns token c0 + lane of the tail
+              if (cols_ok && c0 + lane < tail)
+                combine_row_load(p, (int64_t)s_off[e] + mt * kPairBM + c0 + lane, cr);
+              else
+                combine_row_clear(cr);
+            }
             uint32_t v[32];
             tmem_ld_32x32b_x32(t_row + c0, v);
             tmem_ld_wait();
@@ -593,11 +815,39 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int j = lane + 32 * k, t = j >> 2, part = j & 3;
-              if (cols_ok && c0 + t < tail)
-                *reinterpret_cast<uint4*>(obase + (int64_t)(c0 + t) * p.n_out + col0 + part * 8) =
-                    *reinterpret_cast<const uint4*>(stg + t * 32 + part * 8);
+              if constexpr (FK == 1) {
+                // top-1: the token's row is its unit's output, g·Y straight into y (lane t owns it)
+                const int tu = __shfl_sync(0xffffffffu, cr.t, t);
+                const float g = __shfl_sync(0xffffffffu, cr.g[0], t);
+                const uint4 v = *reinterpret_cast<const uint4*>(stg + t * 32 + part * 8);
+                if (cols_ok && c0 + t < tail && tu >= 0) {
+                  if (p.keep_packed)
+                    *reinterpret_cast<uint4*>(obase + (int64_t)(c0 + t) * p.n_out + col0 + part * 8) = v;
+                  const __nv_bfloat16* pv = reinterpret_cast<const __nv_bfloat16*>(&v);
+                  uint32_t o[4];
+#pragma unroll
+                  for (int i = 0; i < 4; ++i)
+                    o[i] = pack_bf16x2(fmaf(g, __bfloat162float(pv[2 * i]), 0.f),
+                                       fmaf(g, __bfloat162float(pv[2 * i + 1]), 0.f));
+                  *reinterpret_cast<uint4*>(p.y + (int64_t)tu * p.n_out + col0 + part * 8) =
+                      make_uint4(o[0], o[1], o[2], o[3]);
+                }
+              } else {
+                if (cols_ok && c0 + t < tail)
+                  *reinterpret_cast<uint4*>(obase + (int64_t)(c0 + t) * p.n_out + col0 + part * 8) =
+                      *reinterpret_cast<const uint4*>(stg + t * 32 + part * 8);
+              }
             }
             __syncwarp();
+            if constexpr (FK > 1) {
+              // each token's chunk was stored by 4 lanes: all fence before the owners count it
+              __threadfence();
+              __syncwarp();
+              const uint32_t last =
+                  cr.t >= 0 ? combine_arrive(p, cr, p.arrivals + (int64_t)cr.t * (p.n_out >> 5) + (col0 >> 5), 1u)
+                            : 0u;
+              combine_owned<FK, 4>(p, last, cr, col0);
+            }
           }
         }
       } else if (EPI == kEpiSwiGLU) {
@@ -637,9 +887,15 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-            uint4* dst = reinterpret_cast<uint4*>(orow + col);
+            const bool direct = FK > 0 && cr.kept == 1;
+            if (!direct || p.keep_packed) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + col);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+              for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
+            if constexpr (FK > 0) {
+              if (direct) store_direct_x32(p, cr, p.y + (int64_t)cr.t * p.n_out + col, pk);
+            }
           }
         }
       }
@@ -648,6 +904,19 @@ expert_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid
       if (lane == 0) {
         if (leader) mbar_arrive(tempty_bar(acc));
         else mbar_arrive_remote(tempty_leader0 + 8u * acc);
+      }
+      if constexpr (FK > 0) {
+        if (tail > p.swap_max) {  // plain tile: the accumulator is free again; finish the units
+          uint32_t chunks = 0;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            if (nt * kBN + c * 32 < p.n_out) chunks |= 1u << c;
+          const uint32_t last =
+              cr.kept >= 2
+                  ? combine_arrive(p, cr, p.arrivals + (int64_t)cr.t * (p.n_out >> 5) + nt * (kBN / 32), chunks)
+                  : 0u;
+          combine_owned<FK, 32>(p, last, cr, nt * kBN);
+        }
       }
     }
   }
@@ -677,7 +946,7 @@ static int resident_cluster_grid(Kern kern, int cluster, size_t smem, int want) 
   return n * cluster < want ? n * cluster : want;
 }
 
-template <int EPI>
+template <int EPI, int FK>
 static cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                                   const CUtensorMap& s0, const CUtensorMap& s1, const TcParams& p,
                                   int grid, cudaStream_t s, bool pdl) {
@@ -686,47 +955,65 @@ static cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b0, c
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(expert_gemm_tc_pair_kernel<EPI>,
+    cudaError_t e = cudaFuncSetAttribute(expert_gemm_tc_pair_kernel<EPI, FK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmem);
     if (e != cudaSuccess) return e;
-    grid_cap[dev] = resident_cluster_grid(expert_gemm_tc_pair_kernel<EPI>, 2, kPairSmem, grid);
+    grid_cap[dev] = resident_cluster_grid(expert_gemm_tc_pair_kernel<EPI, FK>, 2, kPairSmem, grid);
     attr_done[dev] = true;
   }
   if (dev < 64 && grid_cap[dev] > 0 && grid > grid_cap[dev]) grid = grid_cap[dev];
   // the 2-CTA cluster shape is compiled into the kernel
-  return launch_kernel(expert_gemm_tc_pair_kernel<EPI>, dim3(grid), dim3(kTcThreads), kPairSmem, s, 1, pdl, a, b0, b1,
+  return launch_kernel(expert_gemm_tc_pair_kernel<EPI, FK>, dim3(grid), dim3(kTcThreads), kPairSmem, s, 1, pdl, a, b0, b1,
                        s0, s1, p);
 }
 
+// Choices forced by moe_set_expert_gemm (-1: automatic).
+static std::atomic<int> g_pair_tiles{-1}, g_transposed_tails{-1}, g_fold_combine{-1};
+
+void set_expert_gemm(int pair_tiles, int transposed_tails, int fold) {
+  g_pair_tiles.store(pair_tiles);
+  g_transposed_tails.store(transposed_tails);
+  g_fold_combine.store(fold);
+}
+
+// With K == 1 the fold only redirects each row's store (g·Y into y), so it saves the y_packed
+// round trip and the combine launch. With K >= 2 each row also fences, counts itself in the arrival
+// counters and, if last, loads its unit's other rows: a chain of dependent memory round trips per
+// row that made the epilogue, not the MMA, set the tile rate on every layer measured.
+bool fold_combine(const Problem& p) {
+  const int forced = g_fold_combine.load(std::memory_order_relaxed);
+  if (forced >= 0) return forced == 1;
+  return p.K == 1;
+}
+
 // Pair tiles (256 rows) pay off when experts hold many rows; with few rows per expert (fine-grained
-// layers) the single-CTA 128-row tile wastes less work on ragged tails. MOE_TC_PAIR=0/1 forces it.
+// layers) the single-CTA 128-row tile wastes less work on ragged tails.
 static bool use_pair_tiles(const Problem& p) {
-  const char* v = getenv("MOE_TC_PAIR");
-  if (v && (v[0] == '0' || v[0] == '1') && v[1] == 0) return v[0] == '1';
+  const int forced = g_pair_tiles.load(std::memory_order_relaxed);
+  if (forced >= 0) return forced == 1;
   return p.rows / p.E >= kPairBM;
 }
 
 // Largest tail (rows) that a pair-tile GEMM with reduction length K runs transposed.
-// MOE_TC_SWAP=0/1 forces the transposed tails off/on whatever K is.
 static int swap_max_rows(int K) {
-  const char* v = getenv("MOE_TC_SWAP");
-  if (v && (v[0] == '0' || v[0] == '1') && v[1] == 0) return v[0] == '1' ? kSwapMaxRows : 0;
+  const int forced = g_transposed_tails.load(std::memory_order_relaxed);
+  if (forced >= 0) return forced == 1 ? kSwapMaxRows : 0;
   return (K + kBK - 1) / kBK >= kSwapMinKBlocks ? kSwapMaxRows : 0;
 }
 
-template <int EPI>
+template <int EPI, int FK>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                              const TcParams& p, int grid, cudaStream_t s, bool pdl) {
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(expert_gemm_tc_kernel<EPI>,
+    cudaError_t e = cudaFuncSetAttribute(expert_gemm_tc_kernel<EPI, FK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  return launch_kernel(expert_gemm_tc_kernel<EPI>, dim3(grid), dim3(kTcThreads), kTcSmem, s, 1, pdl, a, b0, b1, p);
+  return launch_kernel(expert_gemm_tc_kernel<EPI, FK>, dim3(grid), dim3(kTcThreads), kTcSmem, s, 1, pdl, a, b0, b1, p);
 }
 
 cudaError_t launch_expert_ffn_simt(const Problem& p, const void* x_packed, const int32_t* offsets,
@@ -736,10 +1023,15 @@ cudaError_t launch_expert_ffn_simt(const Problem& p, const void* x_packed, const
 cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int32_t* offsets,
                               const void* w_gate, const void* w_up, const void* w_down,
                               void* hidden, void* y_packed, uint32_t* status, cudaStream_t s,
-                              void* save_gu, bool pdl) {
-  if (!p.bf16)
+                              void* save_gu, bool pdl, const FusedCombine* fc) {
+  if (!p.bf16) {
+    if (fc) return cudaErrorInvalidValue;  // the combine is folded only into the tensor-core GEMM
     return launch_expert_ffn_simt(p, x_packed, offsets, w_gate, w_up, w_down, hidden, y_packed, status, s, pdl);
+  }
   if (p.rows == 0) return cudaSuccess;
+  if (fc && (!fc->y || !fc->row_token || !fc->slot_of || !fc->gate || !fc->arrivals || p.K > kMaxTopK ||
+             (reinterpret_cast<uintptr_t>(fc->y) & 15) != 0))
+    return cudaErrorInvalidValue;
   CUtensorMap mA, mW1, mW3, mH, mW2;
   const uint64_t rows = (uint64_t)p.rows;
   if (!encode_tmap_2d_bf16(&mA, x_packed, (uint64_t)p.hu, rows, kBK, kBM) ||
@@ -769,10 +1061,10 @@ cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int3
   g.out = static_cast<__nv_bfloat16*>(hidden);
   g.swap_max = swap_max_rows(g.K);
   g.save_gu = static_cast<__nv_bfloat16*>(save_gu);
-  cudaError_t e = pair ? launch_tc_pair<kEpiSwiGLU>(mA, mW1, mW3, mW1s, mW3s, g, grid, s, pdl)
-                       : launch_tc<kEpiSwiGLU>(mA, mW1, mW3, g, grid, s, pdl);
+  cudaError_t e = pair ? launch_tc_pair<kEpiSwiGLU, 0>(mA, mW1, mW3, mW1s, mW3s, g, grid, s, pdl)
+                       : launch_tc<kEpiSwiGLU, 0>(mA, mW1, mW3, g, grid, s, pdl);
   if (e != cudaSuccess) return e;
-  // down → y_packed
+  // down → y_packed (and, folded in, y)
   g.K = p.d_ff;
   g.w_rows = p.hu;
   g.n_tiles = (p.hu + kBN - 1) / kBN;
@@ -780,8 +1072,25 @@ cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int3
   g.out = static_cast<__nv_bfloat16*>(y_packed);
   g.swap_max = swap_max_rows(g.K);
   g.save_gu = nullptr;
-  return pair ? launch_tc_pair<kEpiPlain>(mH, mW2p, mW2p, mW2p, mW2p, g, grid, s, true)
-              : launch_tc<kEpiPlain>(mH, mW2, mW2, g, grid, s, true);
+  if (!fc)
+    return pair ? launch_tc_pair<kEpiPlain, 0>(mH, mW2p, mW2p, mW2p, mW2p, g, grid, s, true)
+                : launch_tc<kEpiPlain, 0>(mH, mW2, mW2, g, grid, s, true);
+  g.y = static_cast<__nv_bfloat16*>(fc->y);
+  g.row_token = fc->row_token;
+  g.slot_of = fc->slot_of;
+  g.gate = fc->gate;
+  g.arrivals = fc->arrivals;
+  g.Tu = p.Tu;
+  g.topk = p.K;
+  g.keep_packed = fc->keep_packed ? 1 : 0;
+  if (p.K == 1)
+    return pair ? launch_tc_pair<kEpiPlain, 1>(mH, mW2p, mW2p, mW2p, mW2p, g, grid, s, true)
+                : launch_tc<kEpiPlain, 1>(mH, mW2, mW2, g, grid, s, true);
+  if (p.K == 2)
+    return pair ? launch_tc_pair<kEpiPlain, 2>(mH, mW2p, mW2p, mW2p, mW2p, g, grid, s, true)
+                : launch_tc<kEpiPlain, 2>(mH, mW2, mW2, g, grid, s, true);
+  return pair ? launch_tc_pair<kEpiPlain, 8>(mH, mW2p, mW2p, mW2p, mW2p, g, grid, s, true)
+              : launch_tc<kEpiPlain, 8>(mH, mW2, mW2, g, grid, s, true);
 }
 
 }  // namespace moe

@@ -147,6 +147,7 @@ WsLayout ws_layout(const Problem& p) {
   L.x_packed = take(rows * (size_t)p.hu * p.elt);
   L.hidden = take(rows * (size_t)p.d_ff * p.elt);
   L.y_packed = take(rows * (size_t)p.hu * p.elt);
+  L.arrivals = take(p.bf16 ? (size_t)p.Tu * (size_t)(p.hu / 32) * 4 : 0);
   L.total = off;
   return L;
 }
@@ -200,6 +201,13 @@ static moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_O
 extern "C" {
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+moe_status_t moe_set_expert_gemm(int32_t pair_tiles, int32_t transposed_tails, int32_t fold_combine) {
+  for (const int32_t v : {pair_tiles, transposed_tails, fold_combine})
+    if (v < -1 || v > 1) return MOE_ERR_INVALID_ARG;
+  set_expert_gemm(pair_tiles, transposed_tails, fold_combine);
+  return MOE_OK;
+}
 
 uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -445,17 +453,25 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const void* x, const m
   if (token_ids && o.aux && cudaMemsetAsync(o.aux, 0, sizeof(float), s) != cudaSuccess) return MOE_ERR_CUDA;
   e = scan_stage(p, ws, o.counts, o.offsets, token_ids ? nullptr : o.aux, s, pdl && !token_ids);
   if (e != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
+  // the combine folded into the down GEMM (K == 1 unless set otherwise): the pack zeroes the
+  // arrival counters and the y rows of units with no kept pick, and no combine launch follows
+  const bool fold = p.bf16 && p.rows > 0 && aligned16(y) && fold_combine(p);
+  uint32_t* arrivals = fold ? ws_ptr<uint32_t>(ws, L.arrivals) : nullptr;
   if (p.rows > 0) {
     e = launch_pack(p, x, idx, kTileShift, ws_ptr<int32_t>(ws, L.chunk_base), offsets_ws, slot_of, row_token, x_packed,
-                    s, pdl);
+                    s, pdl, nullptr, fold ? y : nullptr, arrivals);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (!mark(3)) return MOE_ERR_CUDA;
+  const FusedCombine fc = {y, row_token, slot_of, gate, arrivals, gu != nullptr};
   e = launch_expert_ffn(p, x_packed, offsets_ws, w->w_gate, w->w_up, w->w_down, hidden, y_packed,
-                        status, s, gu, pdl);
+                        status, s, gu, pdl, fold ? &fc : nullptr);
   if (e != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
-  e = launch_combine(p, y_packed, slot_of, gate, y, status, s, pdl);
-  if (e != cudaSuccess || !mark(5)) return MOE_ERR_CUDA;
+  if (!fold) {
+    e = launch_combine(p, y_packed, slot_of, gate, y, status, s, pdl);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (!mark(5)) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

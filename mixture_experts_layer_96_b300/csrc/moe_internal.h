@@ -71,6 +71,7 @@ struct WsLayout {
   size_t x_packed;     // elt [T'K][h']
   size_t hidden;       // elt [T'K][d_ff]
   size_t y_packed;     // elt [T'K][h']
+  size_t arrivals;     // uint32 [T'][h'/32] rows done per unit and 32-column chunk (bf16 layers)
   size_t total;
 };
 
@@ -174,17 +175,33 @@ cudaError_t launch_scan(const Problem& p, int64_t nchunks, const int32_t* hist, 
 // the packed rows.
 cudaError_t launch_pack(const Problem& p, const void* x, const int32_t* idx, int chunk_shift, const int32_t* chunk_base,
                         const int32_t* offsets, int32_t* slot_of, int32_t* row_token, void* x_packed, cudaStream_t s,
-                        bool pdl, const int64_t* cap_e = nullptr);
+                        bool pdl, const int64_t* cap_e = nullptr, void* y_zero = nullptr,
+                        uint32_t* arrivals = nullptr);
 // The whole dispatch from given picks: chunk ranks, scan, pack.
 cudaError_t launch_dispatch_from_idx(const Problem& p, const void* x, const int32_t* idx, int32_t* counts_out,
                                      int32_t* offsets_out, int32_t* slot_of, int32_t* row_token, void* x_packed,
                                      const DispatchScratch& sc, cudaStream_t s);
 
 // save_gu (bf16 layers): also write the SwiGLU inputs G | U as bf16 [rows][2·d_ff] for the backward.
+// moe_set_expert_gemm: forced choices of the expert GEMMs (-1 automatic).
+void set_expert_gemm(int pair_tiles, int transposed_tails, int fold_combine);
+// Whether moe_forward folds the combine into the down GEMM (bf16 layers).
+bool fold_combine(const Problem& p);
+
+// The combine folded into the down GEMM (expert_tc.cu): the down launch also writes y.
+struct FusedCombine {
+  void* y;                   // [T'][h'] layer output
+  const int32_t* row_token;  // [rows] packed row -> unit
+  const int32_t* slot_of;    // [T'][K]
+  const float* gate;         // [T'][K]
+  uint32_t* arrivals;        // [T'][h'/32], zeroed by the pack of the same forward
+  bool keep_packed;          // also leave every Y row in y_packed (the backward reads it)
+};
+
 cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int32_t* offsets,
                               const void* w_gate, const void* w_up, const void* w_down,
                               void* hidden, void* y_packed, uint32_t* status, cudaStream_t s,
-                              void* save_gu = nullptr, bool pdl = false);
+                              void* save_gu = nullptr, bool pdl = false, const FusedCombine* fc = nullptr);
 
 // ---- backward (bf16 layers, h' and d_ff multiples of 64) ---------------------------------------
 cudaError_t launch_expert_ffn_backward(const Problem& p, const int32_t* offsets, const void* x_packed,

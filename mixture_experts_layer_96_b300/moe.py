@@ -26,7 +26,8 @@ EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_capacity", "moe_rout
            "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_status",
            "moe_status_string", "moe_launch_count", "moe_abi_version", "moe_dispatch_noalloc",
            "moe_saved_gu_size", "moe_forward_train", "moe_backward_workspace_size", "moe_backward",
-           "moe_forward_profiled", "moe_route_hash", "moe_forward_hash", "moe_dispatch_sharded")
+           "moe_forward_profiled", "moe_route_hash", "moe_forward_hash", "moe_dispatch_sharded",
+           "moe_set_expert_gemm")
 
 
 class MoEError(RuntimeError):
@@ -104,6 +105,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_status_string": (ctypes.c_char_p, [I32]),
         "moe_launch_count": (ctypes.c_uint64, []),
         "moe_abi_version": (I32, []),
+        "moe_set_expert_gemm": (I32, [I32, I32, I32]),
         "moe_dispatch_noalloc": (I32, [cfgp, P, P, P, P, P, P, P, P]),
         "moe_saved_gu_size": (S, [cfgp]),
         "moe_forward_train": (I32, [cfgp, P, ctypes.POINTER(MoEWeights), P, ctypes.POINTER(MoEOutputs), P, P, P]),
@@ -149,6 +151,14 @@ def capacity(cfg: MoEConfig) -> Optional[int]:
 
 def launch_count() -> int:
     return int(load_library().moe_launch_count())
+
+
+def set_expert_gemm(pair_tiles: int = -1, transposed_tails: int = -1, fold_combine: int = -1) -> None:
+    """Force the expert GEMMs' choices process-wide (1 on, 0 off, -1 automatic): CTA-pair 256-row
+    tiles, transposed pair-tile tails of up to 224 rows, and the combine folded into the down GEMM
+    (automatic: K == 1)."""
+    _check(load_library().moe_set_expert_gemm(int(pair_tiles), int(transposed_tails), int(fold_combine)),
+           "moe_set_expert_gemm")
 
 
 # ------------------------------------------------------------------------------------------------

@@ -3,6 +3,7 @@ tolerances, and the bit-exact routing check on the GPU's own fp32 logits."""
 from __future__ import annotations
 
 import math
+from contextlib import contextmanager
 from dataclasses import dataclass
 from typing import Optional
 
@@ -13,6 +14,26 @@ import oracle.moe_oracle as O
 from workloads import Generator, MoEShape, bf16_bits_to_f32
 
 U32 = 2.0 ** -24  # unit roundoff of fp32
+
+
+TILE_MODES = {  # name -> (pair_tiles, transposed_tails) for set_expert_gemm
+    "single": (0, -1),
+    "pair": (1, -1),
+    "pair_tails_transposed": (1, 1),
+    "pair_tails_plain": (1, 0),
+}
+
+
+@contextmanager
+def expert_tiles(mode: str, fold_combine: int = -1):
+    """Force the expert GEMMs' tile shape (and the combine fold) for the duration (automatic again
+    afterwards)."""
+    from mixture_experts_layer_96_b300 import set_expert_gemm
+    set_expert_gemm(*TILE_MODES[mode], fold_combine)
+    try:
+        yield mode
+    finally:
+        set_expert_gemm(-1, -1, -1)
 
 
 def config_of(shape: MoEShape):

@@ -112,6 +112,21 @@ def test_layer_roofline_dense_workload_is_tensor_bound():
     assert 0.8 < lr["frac_of_forward"] < 1.0
 
 
+def test_layer_roofline_with_the_combine_folded_into_the_down_gemm():
+    """Folded: the expert_ffn stage's time holds the combine too, so it is graded against both
+    rooflines; the combine has no stage fraction of its own; the sum is unchanged."""
+    s = bench.WORKLOADS["multihead_bf16"]
+    kept = s.T_units * s.K
+    stage = {"route": 0.02, "dispatch": 0.04, "expert_ffn": 0.4, "combine": 0.001}
+    plain = bench.layer_roofline(s, kept, 64, stage, 0.5, 7000.0, 1413.0)
+    fold = bench.layer_roofline(s, kept, 64, stage, 0.5, 7000.0, 1413.0, folded=True)
+    assert "combine" not in fold["stage_frac"]
+    both = fold["expert_ffn_ms_at_roofline"] + fold["combine_ms_at_roofline"]
+    assert fold["stage_frac"]["expert_ffn"] == pytest.approx(both / 0.4)
+    assert fold["sum_ms_at_roofline"] == pytest.approx(plain["sum_ms_at_roofline"])
+    assert fold["stage_frac"]["route"] == plain["stage_frac"]["route"]
+
+
 def test_layer_roofline_fine_grained_workload_streams_weights():
     """256 experts of d_ff 2048 at T = 4096: each expert's weights are read for ~128 rows, so the
     GEMMs take longer to stream their weights from HBM than to do their FLOP."""

@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle.moe_backward as B
-from harness import Inputs, as_f64, bits_of, config_of, route_on_gpu_logits, to_device, widen
+from harness import Inputs, as_f64, bits_of, config_of, expert_tiles, route_on_gpu_logits, to_device, widen
 from mixture_experts_layer_96_b300 import (BackwardWorkspace, ForwardOutputs, Workspace, moe_backward,
                                            moe_forward, moe_forward_train)
 from workloads import WORKLOADS, Generator, MoEShape, scaled
@@ -104,14 +104,12 @@ def test_backward_parity_small(shape):
 
 
 @pytest.mark.parametrize("mode", ["single", "pair_tails_transposed", "pair_tails_plain"])
-def test_backward_parity_with_each_forward_tile_mode(mode, monkeypatch):
+def test_backward_parity_with_each_forward_tile_mode(mode):
     """G|U are saved by every forward epilogue: single-CTA tiles, pair tiles, transposed tails."""
-    monkeypatch.setenv("MOE_TC_PAIR", "0" if mode == "single" else "1")
-    if mode != "single":
-        monkeypatch.setenv("MOE_TC_SWAP", "1" if mode == "pair_tails_transposed" else "0")
     shape = scaled(WORKLOADS["mixtral_bf16"], T=900, h=256, d_ff=512)
     inp = Inputs.make(shape)
-    cfg, x, lw, ws, outs, y, gu, dy, bws, g = run_train(inp)
+    with expert_tiles(mode):
+        cfg, x, lw, ws, outs, y, gu, dy, bws, g = run_train(inp)
     idx = gpu_picks_checked(inp, outs)
     check_all(inp, g, oracle_grads(inp, Generator(shape).dy(), idx))
 

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle.moe_oracle as O
-from harness import Inputs, as_f64, bits_of, config_of, route_on_gpu_logits, tol_ok
+from harness import TILE_MODES, Inputs, as_f64, bits_of, config_of, expert_tiles, route_on_gpu_logits, tol_ok
 from mixture_experts_layer_96_b300 import (ForwardOutputs, Workspace, moe_combine, moe_dispatch,
                                            moe_expert_ffn, moe_forward, moe_route)
 from workloads import WORKLOADS, MoEShape, scaled
@@ -197,3 +197,72 @@ def test_profiled_forward_gives_the_same_bits_and_ordered_stage_events():
         assert torch.equal(t1, t2)
     times = [ev[i].elapsed_time(ev[i + 1]) for i in range(5)]
     assert all(t >= 0 for t in times) and sum(times) > 0
+
+
+# ---------------------------------------------------------- combine folded into the down GEMM
+FOLD_CASES = [
+    scaled(WORKLOADS["skewed_bf16"], T=2000, h=256, d_ff=384),             # K = 2, capacity drops
+    MoEShape("switch_top1_cf1.2", T=1000, h=256, E=16, K=1, d_ff=256, capacity_factor=1.2,
+             logit_bias="zipf1.2"),                                       # K = 1: g·Y written directly
+    MoEShape("drop_heavy", T=500, h=128, E=4, K=2, d_ff=128, capacity_factor=0.3,
+             logit_bias="zipf1.2"),                                       # units with no kept pick
+    scaled(WORKLOADS["finegrained_bf16"], T=300, h=512, d_ff=256),        # K = 8, sigmoid, groups
+    MoEShape("e33k5", T=700, h=96, E=33, K=5, d_ff=160),                  # K = 5, ragged widths
+    scaled(WORKLOADS["multihead_bf16"], T=600, h=1024, d_ff=1024),        # H = 4, many 256-row tiles
+    scaled(WORKLOADS["mixtral_bf16"], T=900, h=512, d_ff=1024),
+]
+
+
+@pytest.mark.parametrize("mode", list(TILE_MODES))
+@pytest.mark.parametrize("shape", FOLD_CASES, ids=[s.name for s in FOLD_CASES])
+def test_folded_combine_equals_the_separate_combine(shape, mode):
+    """moe_forward with the combine folded into the down GEMM (forced on for every K: with K >= 2
+    the last row of each unit sums it) must give the bits of the separate stages
+    route → dispatch → expert_ffn → combine, for every tile shape of the down GEMM (plain rows and
+    transposed tails), with every y element written (y starts as NaN)."""
+    inp = Inputs.make(shape)
+    cfg = config_of(shape)
+    x, lw = inp.device()
+    ws = Workspace(cfg)
+    with expert_tiles(mode, fold_combine=1):
+        y = torch.full((shape.T, shape.h), float("nan"), dtype=torch.bfloat16, device="cuda")
+        moe_forward(cfg, x, lw, ws=ws, y=y)
+        y_again = torch.full_like(y, float("nan"))
+        moe_forward(cfg, x, lw, ws=ws, y=y_again)
+        idx, gate, _, _ = moe_route(cfg, x, lw.w_router, lw.logit_bias, lw.select_bias, ws=ws)
+        counts, offsets, slot_of, row_token, xp = moe_dispatch(cfg, x, idx, ws=ws)
+        yp = moe_expert_ffn(cfg, xp, offsets, lw.w_gate, lw.w_up, lw.w_down, ws=ws)
+        y_sep = moe_combine(cfg, yp, slot_of, gate, ws=ws)
+        ws.check()
+    assert not torch.isnan(y.float()).any()
+    assert torch.equal(y.view(torch.int16), y_sep.view(torch.int16))
+    assert torch.equal(y.view(torch.int16), y_again.view(torch.int16))
+    # units none of whose picks was kept are zero
+    dropped = (bits_of(slot_of) < 0).all(axis=1)
+    if dropped.any():
+        yu = y.view(shape.T_units, shape.h_unit)
+        assert not yu[torch.from_numpy(np.nonzero(dropped)[0]).cuda()].any()
+
+
+@pytest.mark.parametrize("K", [1, 2])
+def test_combine_is_folded_automatically_for_top1_only(K):
+    """Automatic choice: a top-1 forward folds the combine into the down GEMM (one launch fewer),
+    a top-2 forward keeps the separate combine launch; both equal the separate stages' bits."""
+    from mixture_experts_layer_96_b300 import launch_count
+    shape = MoEShape(f"top{K}", T=800, h=256, E=16, K=K, d_ff=256, capacity_factor=1.25)
+    inp = Inputs.make(shape)
+    cfg = config_of(shape)
+    x, lw = inp.device()
+    ws = Workspace(cfg)
+    counts = {}
+    ys = {}
+    for fold in (-1, 0):
+        with expert_tiles("single", fold_combine=fold):
+            moe_forward(cfg, x, lw, ws=ws)  # first call outside the count (one-time setup)
+            torch.cuda.synchronize()
+            n0 = launch_count()
+            ys[fold] = moe_forward(cfg, x, lw, ws=ws)
+            counts[fold] = launch_count() - n0
+    ws.check()
+    assert counts[-1] == counts[0] - (1 if K == 1 else 0), counts
+    assert torch.equal(ys[-1].view(torch.int16), ys[0].view(torch.int16))

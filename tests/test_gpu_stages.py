@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle.moe_oracle as O
-from harness import as_f64, bits_of, config_of, to_device, tol_ok, widen
+from harness import TILE_MODES, as_f64, bits_of, config_of, expert_tiles, to_device, tol_ok, widen
 from mixture_experts_layer_96_b300 import (Workspace, moe_combine, moe_dispatch, moe_expert_ffn,
                                            moe_route_logits)
 from workloads import Generator, MoEShape, WORKLOADS, f32_to_bf16_bits, scaled
@@ -127,18 +127,13 @@ FFN_CASES = [
 ]
 
 
-@pytest.fixture(params=["single", "pair", "pair_tails_transposed", "pair_tails_plain"])
-def tile_mode(request, monkeypatch):
+@pytest.fixture(params=list(TILE_MODES))
+def tile_mode(request):
     """Run an expert-FFN case with the single-CTA 128-row tiles and with the CTA-pair 256-row tiles,
     the latter with the automatic choice for experts' last m-tiles and with every tail of up to 224
     rows forced to the transposed tile or to the 256-row tile."""
-    monkeypatch.setenv("MOE_TC_PAIR", "0" if request.param == "single" else "1")
-    swap = {"pair_tails_transposed": "1", "pair_tails_plain": "0"}.get(request.param)
-    if swap is None:
-        monkeypatch.delenv("MOE_TC_SWAP", raising=False)
-    else:
-        monkeypatch.setenv("MOE_TC_SWAP", swap)
-    return request.param
+    with expert_tiles(request.param):
+        yield request.param
 
 
 @pytest.mark.parametrize("shape", FFN_CASES, ids=[s.name for s in FFN_CASES])
