@@ -30,7 +30,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from workloads import WORKLOADS, Generator, bf16_bits_to_f32  # noqa: E402
+from workloads import WORKLOADS, Generator, bf16_bits_to_f32, scaled  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s"
 UNIT = "tokens/s"
@@ -716,7 +716,7 @@ def run_ours(args, shape):
                      "frac_of_burst": achieved_tf / float(pk["bf16_tflops"]),
                      "frac_of_sustained": achieved_tf / float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
                      "algorithmic_flop": flops,
-                     "traffic": recorded_traffic(args.workload),
+                     "traffic": recorded_traffic(args.workload) if args.d_ff is None else None,
                      "traffic_unit": "DRAM bytes per forward (both GEMM launches), ncu",
                      "gemm_source_sha1": gemm_source_sha()},
         "stages": stages,
@@ -780,8 +780,13 @@ def main():
     ap.add_argument("--no-train", dest="train", action="store_false")
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
                     help="keep warming up at least this long (steady clocks); 0 for profiling runs")
+    ap.add_argument("--d-ff", type=int, default=None,
+                    help="replace the workload's d_ff (small cases for profiler captures of the kernels that "
+                         "do not depend on it; the line then names the changed workload)")
     args = ap.parse_args()
     shape = WORKLOADS[args.workload]
+    if args.d_ff is not None:
+        shape = scaled(shape, d_ff=args.d_ff)
     if args.impl == "reference":
         run_reference(args, shape)
     else:

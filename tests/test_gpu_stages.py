@@ -239,6 +239,12 @@ COMBINE_CASES = [
     (scaled(WORKLOADS["multihead_bf16"], T=100, h=1024), 0.3),
     (scaled(WORKLOADS["tiny_f32"], T=256), 1.25),
     (MoEShape("f32_odd", T=50, h=10, E=3, K=2, d_ff=8, dtype="f32"), 1.0),
+    # the bulk-copy combine: K = 8 rows of 14 KB in four segments, many items per block (the
+    # stage ring wraps several times); K = 5 with drops and a shorter last segment; a long batch
+    # of short rows, 24 units per stage
+    (scaled(WORKLOADS["finegrained_bf16"], T=400), None),
+    (MoEShape("k5_three_segments", T=300, h=4160, E=12, K=5, d_ff=64), 1.0),
+    (MoEShape("many_units", T=40000, h=256, E=16, K=2, d_ff=64), 1.25),
 ]
 
 
