@@ -177,6 +177,16 @@ def test_forward_parity_full_size_sampled(name):
     check_forward(inp, y, outs, sample=tile_covering_sample(256))
 
 
+def test_forward_parity_when_the_route_grid_exceeds_two_ctas_per_sm():
+    """More 128-unit tiles than two per SM (T' = 40000, h' = 512: 313 single-CTA tiles), so the
+    routing kernel runs in more than one wave: routing stays bit-exact on the GPU's logits for every
+    unit, and y is checked on a tile-covering sample."""
+    shape = scaled(WORKLOADS["multihead_bf16"], T=10000, d_ff=256)
+    inp = Inputs.make(shape)
+    y, outs = run_forward(inp)
+    check_forward(inp, y, outs, sample=tile_covering_sample(256))
+
+
 def test_profiled_forward_gives_the_same_bits_and_ordered_stage_events():
     """moe_forward_profiled runs the forward's own kernels with an event at each stage boundary: y
     and the outputs equal moe_forward's bit for bit, and the events bracket five stages."""
