@@ -245,11 +245,20 @@ __device__ __forceinline__ void store_direct_x32(const TcParams& p, const Combin
   for (int j = 0; j < 4; ++j) d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
 }
 
+// Single-CTA tiles: an expert's last m-tile of at most kSwapMaxRowsSingle rows runs transposed,
+// Dᵀ = W·Xᵀ, as two M = 128 MMAs over the tile's 256 weight rows with N = the tail's tokens rounded
+// up to a multiple of 16 (both blocks fit one 256-column accumulator). Experts of about 128 rows
+// (fine-grained layers) otherwise spend a mostly empty second 128-row tile.
+constexpr int kSwapMaxRowsSingle = 112;
+__device__ __forceinline__ int swap_tokens(int tail) { return (tail + 15) & ~15; }
+
 template <int EPI, int FK>
 __global__ void __launch_bounds__(kTcThreads, 1)
 expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                       const __grid_constant__ CUtensorMap tmB1, TcParams p) {
   extern __shared__ unsigned char smem_dyn[];
+  // transposed tails: per epilogue warp, a [token][32 columns] bf16 chunk turned into row stores
+  __shared__ __align__(16) __nv_bfloat16 s_stage[4 * 32 * 32];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_pre[kMaxExperts + 1];
   __shared__ __align__(8) uint64_t s_bar[2 * kStages + 5];
@@ -357,15 +366,33 @@ expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) { aborted = true; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
+        int e, mt, nt;
+        decode_tile(tile, s_pre, p.E, p.n_tiles, e, mt, nt);
+        const int tail = s_off[e + 1] - s_off[e] - mt * kBM;
+        const bool swap = tail <= p.swap_max;
+        const int n_tok = swap_tokens(tail);
+        const uint32_t idesc_t = idesc_bf16_f32(kBM, swap ? n_tok : 16);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag)) { aborted = true; break; }
           tc_fence_after();
           const uint32_t sa = sbase + stage * kStageBytes, sb = sa + kABytes;
           const uint64_t ad = sdesc_kmajor_sw128(sa), bd = sdesc_kmajor_sw128(sb);
+          if (!swap) {
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)  // 16 bf16 = 32 bytes per MMA along K
-            umma_bf16(d_tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), kIdesc,
-                      (kb > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kBK / 16; ++k)  // 16 bf16 = 32 bytes per MMA along K
+              umma_bf16(d_tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), kIdesc,
+                        (kb > 0 || k > 0) ? 1u : 0u);
+          } else {
+            // Dᵀ: weight rows 0-127 of the tile into columns [0, n_tok), rows 128-255 into
+            // [n_tok, 2·n_tok); the tail's tokens (the first n_tok of the 128 loaded) are N
+            const uint64_t bd1 = sdesc_kmajor_sw128(sb + kBBytes / 2);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              umma_bf16(d_tmem, bd + (uint64_t)(2 * k), ad + (uint64_t)(2 * k), idesc_t, (kb > 0 || k > 0) ? 1u : 0u);
+              umma_bf16(d_tmem + (uint32_t)n_tok, bd1 + (uint64_t)(2 * k), ad + (uint64_t)(2 * k), idesc_t,
+                        (kb > 0 || k > 0) ? 1u : 0u);
+            }
+          }
           umma_commit(empty_bar(stage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -405,7 +432,60 @@ expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       tc_fence_after();
       __nv_bfloat16* orow = p.out + (int64_t)(s_off[e] + r_local) * p.n_out;
       const uint32_t t_row = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(q * 32) << 16);
-      if (EPI == kEpiSwiGLU) {
+      const int tail = rows_e - mt * kBM;
+      if (tail <= p.swap_max) {
+        // transposed tile: TMEM lane = output column (32 per warp), column = token of the tail;
+        // block 0 (columns [0, n_tok)) holds weight rows 0-127 of the tile, block 1 rows 128-255:
+        // for gate/up the gate and the up of the same output column, for down two column halves.
+        // Each chunk of 32 tokens goes through the warp's staging area into 16-byte row pieces.
+        const int n_tok = swap_tokens(tail);
+        __nv_bfloat16* obase = p.out + (int64_t)(s_off[e] + mt * kBM) * p.n_out;
+        __nv_bfloat16* stg = s_stage + (warp - 2) * 32 * 32;
+#pragma unroll 1
+        for (int c0 = 0; c0 < n_tok; c0 += 32) {
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(t_row + c0, v0);
+          tmem_ld_32x32b_x32(t_row + n_tok + c0, v1);
+          tmem_ld_wait();
+          // out: 0 = SwiGLU H (or down block 0), 1 = down block 1; then G and U for the backward
+          const int nout = EPI == kEpiSwiGLU ? (p.save_gu != nullptr ? 3 : 1) : 2;
+#pragma unroll 1
+          for (int w = 0; w < nout; ++w) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float g = __uint_as_float(v0[i]), u = __uint_as_float(v1[i]);
+              float val;
+              if (EPI == kEpiSwiGLU) val = w == 0 ? silu_f32(g) * u : (w == 1 ? g : u);
+              else val = w == 0 ? g : u;
+              stg[i * 32 + lane] = __float2bfloat16_rn(val);
+            }
+            __syncwarp();
+            __nv_bfloat16* dbase;
+            int64_t ld;
+            int col0;
+            if (EPI == kEpiSwiGLU) {
+              col0 = nt * 128 + q * 32;
+              if (w == 0) { dbase = obase; ld = p.n_out; }
+              else {
+                dbase = p.save_gu + (int64_t)(s_off[e] + mt * kBM) * (2 * p.n_out) + (w == 2 ? p.n_out : 0);
+                ld = 2 * (int64_t)p.n_out;
+              }
+            } else {
+              col0 = nt * kBN + w * 128 + q * 32;
+              dbase = obase;
+              ld = p.n_out;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int j = lane + 32 * k, t = j >> 2, part = j & 3;
+              if (col0 < p.n_out && c0 + t < tail)
+                *reinterpret_cast<uint4*>(dbase + (int64_t)(c0 + t) * ld + col0 + part * 8) =
+                    *reinterpret_cast<const uint4*>(stg + t * 32 + part * 8);
+            }
+            __syncwarp();
+          }
+        }
+      } else if (EPI == kEpiSwiGLU) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t g[32], u[32];
@@ -994,11 +1074,12 @@ static bool use_pair_tiles(const Problem& p) {
   return p.rows / p.E >= kPairBM;
 }
 
-// Largest tail (rows) that a pair-tile GEMM with reduction length K runs transposed.
-static int swap_max_rows(int K) {
+// Largest tail (rows) that a GEMM with reduction length K runs transposed (pair or single tiles).
+static int swap_max_rows(int K, bool pair) {
+  const int most = pair ? kSwapMaxRows : kSwapMaxRowsSingle;
   const int forced = g_transposed_tails.load(std::memory_order_relaxed);
-  if (forced >= 0) return forced == 1 ? kSwapMaxRows : 0;
-  return (K + kBK - 1) / kBK >= kSwapMinKBlocks ? kSwapMaxRows : 0;
+  if (forced >= 0) return forced == 1 ? most : 0;
+  return (K + kBK - 1) / kBK >= kSwapMinKBlocks ? most : 0;
 }
 
 template <int EPI, int FK>
@@ -1059,7 +1140,7 @@ cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int3
   g.n_tiles = (p.d_ff + kBN / 2 - 1) / (kBN / 2);
   g.n_out = p.d_ff;
   g.out = static_cast<__nv_bfloat16*>(hidden);
-  g.swap_max = swap_max_rows(g.K);
+  g.swap_max = swap_max_rows(g.K, pair);
   g.save_gu = static_cast<__nv_bfloat16*>(save_gu);
   cudaError_t e = pair ? launch_tc_pair<kEpiSwiGLU, 0>(mA, mW1, mW3, mW1s, mW3s, g, grid, s, pdl)
                        : launch_tc<kEpiSwiGLU, 0>(mA, mW1, mW3, g, grid, s, pdl);
@@ -1070,7 +1151,7 @@ cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int3
   g.n_tiles = (p.hu + kBN - 1) / kBN;
   g.n_out = p.hu;
   g.out = static_cast<__nv_bfloat16*>(y_packed);
-  g.swap_max = swap_max_rows(g.K);
+  g.swap_max = swap_max_rows(g.K, pair);
   g.save_gu = nullptr;
   if (!fc)
     return pair ? launch_tc_pair<kEpiPlain, 0>(mH, mW2p, mW2p, mW2p, mW2p, g, grid, s, true)
@@ -1083,6 +1164,7 @@ cudaError_t launch_expert_ffn(const Problem& p, const void* x_packed, const int3
   g.Tu = p.Tu;
   g.topk = p.K;
   g.keep_packed = fc->keep_packed ? 1 : 0;
+  if (!pair) g.swap_max = 0;  // the single-CTA transposed epilogue does not fold the combine
   if (p.K == 1)
     return pair ? launch_tc_pair<kEpiPlain, 1>(mH, mW2p, mW2p, mW2p, mW2p, g, grid, s, true)
                 : launch_tc<kEpiPlain, 1>(mH, mW2, mW2, g, grid, s, true);

@@ -18,6 +18,8 @@ U32 = 2.0 ** -24  # unit roundoff of fp32
 
 TILE_MODES = {  # name -> (pair_tiles, transposed_tails) for set_expert_gemm
     "single": (0, -1),
+    "single_tails_transposed": (0, 1),
+    "single_tails_plain": (0, 0),
     "pair": (1, -1),
     "pair_tails_transposed": (1, 1),
     "pair_tails_plain": (1, 0),

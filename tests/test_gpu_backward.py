@@ -103,7 +103,8 @@ def test_backward_parity_small(shape):
     check_all(inp, g, ref)
 
 
-@pytest.mark.parametrize("mode", ["single", "pair_tails_transposed", "pair_tails_plain"])
+@pytest.mark.parametrize("mode", ["single_tails_transposed", "single_tails_plain", "pair_tails_transposed",
+                                  "pair_tails_plain"])
 def test_backward_parity_with_each_forward_tile_mode(mode):
     """G|U are saved by every forward epilogue: single-CTA tiles, pair tiles, transposed tails."""
     shape = scaled(WORKLOADS["mixtral_bf16"], T=900, h=256, d_ff=512)

@@ -130,8 +130,8 @@ FFN_CASES = [
 @pytest.fixture(params=list(TILE_MODES))
 def tile_mode(request):
     """Run an expert-FFN case with the single-CTA 128-row tiles and with the CTA-pair 256-row tiles,
-    the latter with the automatic choice for experts' last m-tiles and with every tail of up to 224
-    rows forced to the transposed tile or to the 256-row tile."""
+    each with the automatic choice for experts' last m-tiles and with every tail (up to 112 rows
+    single, 224 pair) forced to the transposed tile or to the plain tile."""
     with expert_tiles(request.param):
         yield request.param
 
