@@ -176,3 +176,14 @@ def test_gradient_buffers_are_fp32_except_dx():
     with pytest.raises(ValueError, match="CUDA device"):
         g.check(cfg)
     assert M.Grads.allocate(cfg, "cpu", extras=False).dlogits is None
+
+
+def test_expert_gemm_choices_are_validated_on_host():
+    """moe_set_expert_gemm takes 1, 0 or -1 for each choice (host only, nothing launched); other
+    values are refused and leave the automatic choices in place."""
+    from mixture_experts_layer_96_b300 import MoEError, set_expert_gemm
+    for bad in [(2, -1, -1), (-1, -2, -1), (-1, -1, 5)]:
+        with pytest.raises(MoEError):
+            set_expert_gemm(*bad)
+    set_expert_gemm(1, 0, 1)
+    set_expert_gemm(-1, -1, -1)
